@@ -1,0 +1,553 @@
+#!/usr/bin/env python
+"""Benchmark of ReplaySSM ring spec-verify for one Gated DeltaNet layer.
+
+Metric: verified tokens/s per GDN layer, and the verify kernel's achieved HBM
+GB/s against the measured roofline, on one GB300.
+
+Workload (default): the Qwen3-Next-shaped layer (H=16 q/k heads, HV=32 v-heads,
+K=V=128, bf16 I/O, fp32 checkpoint, draft window T=4, ring L=64) at B=128 rows
+scattered in a 512-slot pool.  State is built by the library itself: 16 prefix
+rounds (64 tokens, all accepted) from a zero checkpoint, then 48 rounds with
+accept_len ~ U{1..4} so that the slots' ring fill levels spread out.  All inputs
+are seeded synthetic tensors (the pages measure on served models and datasets,
+which are not available here).
+
+A step is one decode round of the layer: verify (output of the whole draft
+window, ring side channel) -> commit(accept_len) -> fold (exact, only slots whose
+is_flush is set; cursors move after).  Steps are captured in CUDA graphs and
+timed with CUDA events; timing events inside the graph bracket every verify, so
+the verify kernel's own duration is measured in the timed region.  The
+checkpoint working set (B x 32 x 64 KiB = 256 MiB at B=128) exceeds L2.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tokens/s per GDN layer and achieved HBM GB/s vs roofline, 1×GB300"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------- accounting
+
+def verify_bytes_per_unit(W: np.ndarray, K: int, V: int, T: int, G: int, e: int,
+                          per_key: bool) -> np.ndarray:
+    """Algorithmic HBM bytes one verify must move per (row, v-head) unit with W
+    committed-but-unfolded ring records: checkpoint read, history records,
+    window inputs, outputs and the ring write of the window."""
+    gbytes = 4 * K if per_key else 4
+    rec = V * e + K * e / G + gbytes + 4                  # rawv + rawk share + g + beta
+    win_in = 2 * K * e / G + V * e + (K * e if per_key else e) + e   # q, k share, v, a, b
+    return V * K * 4 + W * rec + T * win_in + T * V * e + T * rec
+
+
+def mirror_cursors(wp, base, acc_rows, T, L):
+    """Host copy of the cursor arithmetic (commit then fold), used only to know
+    each verify's ring fill W for byte accounting.  Returns W per step [steps, B]."""
+    wp = wp.astype(np.int64).copy()
+    out = []
+    for acc in acc_rows:
+        out.append(wp.copy())
+        wp = wp + acc
+        flush = wp + 2 * T > L
+        wp[flush] = 0
+    return np.array(out)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_delta_rule_spec_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("verify") or name == "common.cuh":
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(path_name: str, B: int):
+    """DRAM bytes per verify launch from the committed ncu summary, if it was
+    taken on the current verify source; else None."""
+    f = os.path.join(ROOT, "profiles", f"verify_{path_name}_traffic.json")
+    if not os.path.exists(f):
+        return None
+    try:
+        rec = json.load(open(f))
+    except Exception:
+        return None
+    if rec.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    per_row = rec.get("dram_bytes_per_launch_per_row")
+    return None if per_row is None else float(per_row) * B
+
+
+def measured_peaks():
+    f = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(f):
+        return json.load(open(f)), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (stamped on arrival) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        rows = [s for t, s in self.samples if t0 <= t <= t1]
+        if not rows:  # short region: take the nearest samples around it
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            rows = [s for _, s in near[:3]]
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[0]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": num(rows[0][1]),
+                "power_w_max": max(num(r[2]) for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ----------------------------------------------------------------- our arm
+
+class Workload:
+    def __init__(self, B: int):
+        from gated_delta_rule_spec_gb300 import inputs as gen
+        c = gen.WORKLOADS["C2"]
+        self.name = f"qwen3next-gdn-verify-b{B}"
+        self.B, self.H, self.HV, self.K, self.V, self.T, self.L = B, c.H, c.HV, c.K, c.V, c.T, c.L
+        self.num_slots = max(c.num_slots, B)
+        self.G = self.HV // self.H
+        self.e = 2
+
+    def config(self, extra=None):
+        d = {"workload": self.name, "model_layer": "Qwen3-Next-shaped GDN layer",
+             "B": self.B, "H": self.H, "HV": self.HV, "K": self.K, "V": self.V, "T": self.T,
+             "L": self.L, "num_slots": self.num_slots, "io_dtype": "bf16",
+             "state_dtype": "fp32", "step": "verify+commit+fold",
+             "l2": "inputs larger than L2 (checkpoint working set "
+                   f"{self.B * self.HV * self.V * self.K * 4 >> 20} MiB per step)",
+             "parallelism": "replicas"}
+        if extra:
+            d.update(extra)
+        return d
+
+
+def build_state(wl: Workload, seed: int, device):
+    """Layer state built by the library's own rounds from a zero checkpoint."""
+    import torch
+    from gated_delta_rule_spec_gb300 import binding
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    rng = gen.rng_for(seed, "bench", wl.B)
+    layer = binding.SpecLayer(wl.H, wl.HV, wl.K, wl.V, wl.T, wl.L, wl.num_slots, device=device)
+    cur = binding.SpecCursors(wl.num_slots, device=device)
+    A_log, dt_bias = gen.layer_params(rng, wl.HV, wl.K, False)
+    A_log = torch.from_numpy(A_log).to(device)
+    dt_bias = torch.from_numpy(dt_bias).to(device)
+    slots = torch.from_numpy(gen.scattered_slots(rng, wl.num_slots, wl.B)).to(device)
+
+    def dev_window():
+        w = gen.window_inputs(rng, wl.B, wl.T, wl.H, wl.HV, wl.K, wl.V, gen.BF16)
+        return {n: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+                for n, x in w.items()}
+
+    binding.reset(cur, slots)
+    full = torch.full((wl.B,), wl.T, dtype=torch.int32, device=device)
+    for r in range(16 + 48):
+        w = dev_window()
+        binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias)
+        acc = full if r < 16 else torch.from_numpy(gen.accept_lens(rng, wl.B, wl.T)).to(device)
+        binding.commit(cur, wl.T, wl.L, slots, acc)
+        binding.fold(layer, cur, slots)
+    torch.cuda.synchronize()
+    return rng, layer, cur, A_log, dt_bias, slots, dev_window
+
+
+def run_ours(args, rank: int, world: int) -> dict | None:
+    import torch
+    import torch.distributed as dist
+    from gated_delta_rule_spec_gb300 import binding
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    wl = Workload(args.batch)
+    rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 1000 + rank, device)
+    path = binding.verify_path(layer)
+
+    NI = 16
+    R = max(1, min(args.steps, 200))
+    inputs = [dev_window() for _ in range(NI)]
+    acc_np = np.stack([gen.accept_lens(rng, wl.B, wl.T) for _ in range(R)])
+    acc_dev = torch.from_numpy(acc_np).to(device)
+    try:
+        ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(R)]
+    except TypeError:  # torch without external events: time verify in its own graph below
+        ev = None
+
+    def step(i, timed_events=True):
+        w = inputs[i % NI]
+        if timed_events and ev is not None:
+            ev[i][0].record()
+        binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias,
+                       out=outs[i % NI])
+        if timed_events and ev is not None:
+            ev[i][1].record()
+        binding.commit(cur, wl.T, wl.L, slots, acc_dev[i % R])
+        binding.fold(layer, cur, slots)
+
+    outs = [torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device)
+            for _ in range(NI)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graphs = {}
+    with torch.cuda.stream(side):
+        for name, n in (("warm", args.warmup), ("chunk", R), ("rem", args.steps % R)):
+            if n == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    step(i, timed_events=(name == "chunk"))
+            graphs[name] = g
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    # the capture ran nothing; cursors are as build_state left them
+    if "warm" in graphs:
+        graphs["warm"].replay()
+    torch.cuda.synchronize()
+    wp0 = cur.write_pos[slots.long()].cpu().numpy()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record()
+    for _ in range(args.steps // R):
+        graphs["chunk"].replay()
+    if "rem" in graphs:
+        graphs["rem"].replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    # per-verify durations of the last chunk replay inside the timed region
+    verify_ms = []
+    if args.steps // R > 0 and ev is not None:
+        try:
+            verify_ms = [a.elapsed_time(b) for a, b in ev]
+        except RuntimeError:
+            verify_ms = []
+    if not verify_ms:
+        verify_ms = verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias)
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    status = binding.read_status(cur)
+
+    # byte accounting for the verifies of the last chunk replay
+    acc_seq = np.array([acc_np[i % R] for i in range(args.warmup)]
+                       + [acc_np[i % R] for i in range(R)] * (args.steps // R)
+                       + [acc_np[i % R] for i in range(args.steps % R)])
+    # W per step from the cursors read before the timed region (after warm-up)
+    W_all = mirror_cursors(wp0, None, acc_seq[args.warmup:], wl.T, wl.L)
+    last = slice((args.steps // R - 1) * R, (args.steps // R) * R)
+    W_last = W_all[last] if args.steps // R > 0 else W_all
+    bytes_per_launch = float(np.mean([
+        verify_bytes_per_unit(Wr, wl.K, wl.V, wl.T, wl.G, wl.e, False).sum() * wl.HV
+        for Wr in W_last]))
+    mean_W = float(W_last.mean())
+
+    # e2e through the binding with host buffers: H2D inputs, D2H outputs, every step
+    host_in = [{n: t.cpu().pin_memory() for n, t in inputs[i].items()} for i in range(4)]
+    host_acc = torch.from_numpy(acc_np).pin_memory()
+    host_out = torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16).pin_memory()
+    dev_in = {n: torch.empty_like(t) for n, t in inputs[0].items()}
+    dev_acc = torch.empty(wl.B, dtype=torch.int32, device=device)
+    dev_out = torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0].values()) + wl.B * 4
+    d2h = host_out.numel() * host_out.element_size()
+    K_e2e = max(3, min(args.steps, 200))
+
+    def e2e_step(i):
+        src = host_in[i % 4]
+        for n in dev_in:
+            dev_in[n].copy_(src[n], non_blocking=True)
+        dev_acc.copy_(host_acc[i % R], non_blocking=True)
+        binding.verify(layer, cur, slots, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["a"],
+                       dev_in["b"], A_log, dt_bias, out=dev_out)
+        binding.commit(cur, wl.T, wl.L, slots, dev_acc)
+        binding.fold(layer, cur, slots)
+        host_out.copy_(dev_out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K_e2e):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    if world > 1:
+        ms, e2e_ms = reduce_max([ms, e2e_ms], device)
+    if rank != 0:
+        return None
+
+    tokens = world * wl.B * wl.T * args.steps
+    value = tokens / (ms / 1e3)
+    peaks, peak_kind = measured_peaks()
+    v_ms = float(np.mean(verify_ms)) if verify_ms else float("nan")
+    achieved = bytes_per_launch / (v_ms / 1e3) / 1e9 if verify_ms else float("nan")
+    traffic = profiled_traffic(path, wl.B)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
+        "config": wl.config({"verify_kernel": path, "mean_ring_fill_W": round(mean_W, 2)}),
+        "e2e": {"value": round(world * wl.B * wl.T * K_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "steps": K_e2e, "api": "python binding -> C ABI, host pinned buffers"},
+        "gpu_launches": 4 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": round(bytes_per_launch),
+                     "kernel": f"verify ({path})", "peak_kind": peak_kind,
+                     "verify_us": round(v_ms * 1e3, 2)},
+        "verify_tokens_per_s": round(wl.B * wl.T / (v_ms / 1e3), 1) if verify_ms else None,
+        "device_status": status,
+        "clocks": clocks,
+    }
+    return line
+
+
+def reduce_max(values, device="cpu"):
+    """Max over ranks of each value (the job time is the slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias, n=20, reps=10):
+    """Median over replays of a graph of n back-to-back verify calls, per call (ms)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(n):
+                w = inputs[i % len(inputs)]
+                binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log,
+                               dt_bias, out=outs[i % len(outs)])
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / n)
+    return [statistics.median(times)]
+
+
+def cpu_baseline(B: int, seconds: float = 10.0) -> dict:
+    """The fp64 oracle, as it stands, on the host cores: verify of a sample of
+    the workload's rows (all heads), ring fill W ~ U[0, L-2T] as in the sweep."""
+    import oracle
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    c = gen.WORKLOADS["C2"]
+    rows = min(B, 16)
+    rng = gen.rng_for(7, "cpu-baseline", rows)
+    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
+    ring = gen.garbage_ring(rng, rows, c.H, c.HV, c.L, c.K, c.V, gen.BF16)
+    ly = oracle.Layer(d, checkpoint=rng.standard_normal((rows, c.HV, c.V, c.K)) * 0.1,
+                      rawv=gen.to_f64(ring["rawv"]), rawk=gen.to_f64(ring["rawk"]),
+                      ring_g=-np.abs(ring["g"].astype(np.float64)),
+                      ring_beta=np.abs(ring["beta"].astype(np.float64)) % 1.0)
+    wp, base, flag = gen.random_cursors(rng, rows, c.L, c.T)
+    cur = oracle.Cursors(rows, wp, base, flag)
+    A_log, dt = gen.layer_params(rng, c.HV, c.K, False)
+    w = {n: gen.to_f64(x) for n, x in
+         gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16).items()}
+    cores = os.cpu_count() or 1
+    slot_idx = np.arange(rows, dtype=np.int32)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
+                      nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 10000:
+            break
+    return {"value": round(rows * c.T * reps / el, 2), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{rows} rows x {c.HV} v-heads of the B={B} workload, fp64 verify, "
+                      f"{reps} repetitions in {el:.1f} s, W ~ U[0, {c.L - 2 * c.T}]"}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, rank: int, world: int) -> dict | None:
+    """fp64 oracle steps (verify -> commit -> fold) on a bounded sample of the
+    workload's rows, timed on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    wl = Workload(args.batch)
+    c = gen.WORKLOADS["C2"]
+    rows = 2
+    rng = gen.rng_for(11, "reference-arm", rows)
+    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
+    ring = gen.garbage_ring(rng, rows, c.H, c.HV, c.L, c.K, c.V, gen.BF16)
+    ly = oracle.Layer(d, checkpoint=rng.standard_normal((rows, c.HV, c.V, c.K)) * 0.1,
+                      rawv=gen.to_f64(ring["rawv"]), rawk=gen.to_f64(ring["rawk"]),
+                      ring_g=-np.abs(ring["g"].astype(np.float64)),
+                      ring_beta=np.abs(ring["beta"].astype(np.float64)) % 1.0)
+    wp, base, flag = gen.random_cursors(rng, rows, c.L, c.T)
+    cur = oracle.Cursors(rows, wp, base, flag)
+    A_log, dt = gen.layer_params(rng, c.HV, c.K, False)
+    slot_idx = np.arange(rows, dtype=np.int32)
+    cores = os.cpu_count() or 1
+    wins = [{n: gen.to_f64(x) for n, x in
+             gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16).items()}
+            for _ in range(4)]
+    accs = [gen.accept_lens(rng, rows, c.T) for _ in range(4)]
+
+    def step(i):
+        w = wins[i % 4]
+        oracle.verify(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
+                      nthreads=cores)
+        oracle.commit(d, cur, slot_idx, accs[i % 4])
+        oracle.fold(d, ly, cur, slot_idx, nthreads=cores)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    value = rows * c.T * args.steps / el
+    sample = (f"{rows} rows x {c.HV} v-heads of the B={args.batch} workload per step "
+              f"(verify + commit + fold, fp64), {args.steps} steps")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": wl.config({"sample_rows_per_step": rows}),
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--batch", type=int, default=128)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if args.impl == "reference":
+            backend = "gloo"
+        dist.init_process_group(backend)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+        if line is not None and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.batch)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -109,6 +109,8 @@ def _load(path: str | None = None):
         _lib.orc_reset.argtypes = [P, P, P, ctypes.c_int]
         _lib.orc_run.restype = None
         _lib.orc_run.argtypes = [P, P, ctypes.c_int, P, P, P, P]
+        _lib.orc_run_batch.restype = None
+        _lib.orc_run_batch.argtypes = [P, ctypes.c_int, P, ctypes.c_int, P, P, P, P, ctypes.c_int]
     return _lib
 
 
@@ -266,6 +268,18 @@ def run(dims: Dims, S, v, k_raw, g, beta):
     n = v.shape[0]
     _load().orc_run(ctypes.byref(dims._c()), _ptr(S), n, _ptr(v), _ptr(k_raw), _ptr(g),
                     _ptr(beta))
+    return S
+
+
+def run_batch(dims: Dims, S, v, k_raw, g, beta, nthreads: int = 1):
+    """Independent recurrences for many units at once (threads over units).
+    S [U, V, K]; v [U, n, V]; k_raw [U, n, K]; g [U, n] or [U, n, K]; beta [U, n].
+    Returns the new states [U, V, K]."""
+    S = _f64(np.array(S, dtype=np.float64, copy=True))
+    v, k_raw, g, beta = _f64(v), _f64(k_raw), _f64(g), _f64(beta)
+    U, n = v.shape[0], v.shape[1]
+    _load().orc_run_batch(ctypes.byref(dims._c()), U, _ptr(S), n, _ptr(v), _ptr(k_raw), _ptr(g),
+                          _ptr(beta), int(nthreads))
     return S
 
 

@@ -470,3 +470,48 @@ void orc_run(const orc_dims *d, double *S, int n, const double *v, const double 
         orc_step(d->V, d->K, d->per_key_gate, S, v + (size_t)t * d->V,
                  k_raw + (size_t)t * d->K, g + (size_t)t * gw, beta[t], d->l2_eps);
 }
+
+/* Many independent runs at once (one per unit), spread over threads.
+ * S: [nunits, V, K]; v: [nunits, n, V]; k_raw: [nunits, n, K];
+ * g: [nunits, n, gw]; beta: [nunits, n]. */
+typedef struct {
+    const orc_dims *d;
+    int nunits, n;
+    double *S;
+    const double *v, *k_raw, *g, *beta;
+    int next;
+    pthread_mutex_t lock;
+} run_job;
+
+static void *run_worker(void *arg)
+{
+    run_job *J = (run_job *)arg;
+    const orc_dims *d = J->d;
+    const size_t gw = g_width(d), VK = (size_t)d->V * d->K;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int u = J->next++;
+        pthread_mutex_unlock(&J->lock);
+        if (u >= J->nunits) break;
+        orc_run(d, J->S + (size_t)u * VK, J->n, J->v + (size_t)u * J->n * d->V,
+                J->k_raw + (size_t)u * J->n * d->K, J->g + (size_t)u * J->n * gw,
+                J->beta + (size_t)u * J->n);
+    }
+    return NULL;
+}
+
+void orc_run_batch(const orc_dims *d, int nunits, double *S, int n, const double *v,
+                   const double *k_raw, const double *g, const double *beta, int nthreads)
+{
+    run_job J;
+    memset(&J, 0, sizeof J);
+    J.d = d; J.nunits = nunits; J.n = n; J.S = S; J.v = v; J.k_raw = k_raw; J.g = g; J.beta = beta;
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, run_worker, &J);
+    run_worker(&J);
+    for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+}

@@ -1,0 +1,220 @@
+"""Mirror one layer's state between the fp64 oracle and the CUDA library.
+
+Both sides start from the same bytes: the seeded generator draws every input
+in its storage dtype; the oracle sees their exact fp64 values, the GPU the
+bytes themselves.  The checkpoint of each used slot comes from the oracle's
+fp64 recurrence over a prefix, rounded to fp32 (no value ever comes from the
+GPU).  Unused slots and ring positions hold a random garbage template, so a
+full-tensor compare catches writes to the wrong slot, position or head.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from gated_delta_rule_spec_gb300 import binding
+from gated_delta_rule_spec_gb300 import inputs as gen
+
+NTHREADS = max(1, min(16, os.cpu_count() or 1))
+
+# Acceptance bars (the benchmark spec's tolerances, plus the pages' g/beta bound).
+OUT_TOL_BF16 = 3e-2      # max-abs output error, bf16 I/O
+OUT_TOL_FP32 = 1e-4      # fp32 I/O: the error is reported; this is a guard rail
+GATE_TOL = 5e-5          # ring g / beta vs the oracle (prhub report of PR #33102, anchor 3)
+CKPT_REL_FRO = 1e-3      # folded checkpoint, relative Frobenius error
+
+
+def to_dev(x: np.ndarray) -> torch.Tensor:
+    if x.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    if x.dtype == np.float32:
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    if x.dtype == np.int32:
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    raise TypeError(x.dtype)
+
+
+def to_host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.contiguous().cpu().numpy()
+
+
+class Scenario:
+    """One layer, its cursors and a fixed set of batch rows, on both sides."""
+
+    def __init__(self, wl: gen.Workload, B: int, seed: int = 0, num_slots: int | None = None,
+                 slot_idx: np.ndarray | None = None, random_cursors: bool = False,
+                 prefix: int | None = None, decay_shift: float = 0.0, scale: float = 1.0):
+        self.wl = wl
+        self.B = B
+        self.num_slots = num_slots or (B + 1)
+        self.rng = gen.rng_for(seed, wl.name, B, self.num_slots)
+        r = self.rng
+        d = self.dims = oracle.Dims(H=wl.H, HV=wl.HV, K=wl.K, V=wl.V, T=wl.T, L=wl.L,
+                                    num_slots=self.num_slots, per_key_gate=wl.per_key_gate,
+                                    scale=scale)
+        self.io = wl.io_dtype
+        self.G = wl.HV // wl.H
+        self.decay_shift = decay_shift   # subtracted from a: weaker decays
+        self.A_log, self.dt_bias = gen.layer_params(r, d.HV, d.K, d.per_key_gate)
+        if slot_idx is None:
+            slot_idx = (gen.scattered_slots(r, self.num_slots, B) if self.num_slots > B
+                        else np.arange(B, dtype=np.int32))
+        self.slot_idx = np.asarray(slot_idx, np.int32)
+        used = sorted({int(s) for s in self.slot_idx if 0 <= s < self.num_slots})
+
+        ring = gen.garbage_ring(r, d.num_slots, d.H, d.HV, d.L, d.K, d.V, self.io, d.per_key_gate)
+        ckpt = (r.standard_normal((d.num_slots, d.HV, d.V, d.K), dtype=np.float32) * 0.1)
+        if random_cursors:
+            wp, base, flag = gen.random_cursors(r, d.num_slots, d.L, d.T)
+        else:
+            wp = np.zeros(d.num_slots, np.int32)
+            base = np.zeros(d.num_slots, np.int32)
+            flag = np.zeros(d.num_slots, np.int32)
+        pre = wl.prefix if prefix is None else prefix
+        if used and pre > 0:
+            ckpt[used] = self._prefix_states(used, pre).astype(np.float32)
+        if random_cursors and used:
+            self._fill_history(ring, used, wp, base)
+        self.ring0 = {k2: v2.copy() for k2, v2 in ring.items()}
+
+        # oracle side (fp64 of the same values)
+        self.orc = oracle.Layer(d, checkpoint=ckpt.astype(np.float64),
+                                rawv=gen.to_f64(ring["rawv"]), rawk=gen.to_f64(ring["rawk"]),
+                                ring_g=ring["g"].astype(np.float64),
+                                ring_beta=ring["beta"].astype(np.float64))
+        self.orc_cur = oracle.Cursors(d.num_slots, wp.copy(), base.copy(), flag.copy())
+        # device side (the same bytes)
+        self.layer = binding.SpecLayer(d.H, d.HV, d.K, d.V, d.T, d.L, d.num_slots,
+                                       per_key_gate=d.per_key_gate, io_dtype=self.io,
+                                       scale=scale)
+        self.layer.checkpoint.copy_(to_dev(ckpt))
+        self.layer.rawv.copy_(to_dev(ring["rawv"]))
+        self.layer.rawk.copy_(to_dev(ring["rawk"]))
+        self.layer.ring_g.copy_(to_dev(ring["g"]))
+        self.layer.ring_beta.copy_(to_dev(ring["beta"]))
+        self.cur = binding.SpecCursors(d.num_slots)
+        self.cur.write_pos.copy_(to_dev(wp))
+        self.cur.cache_base.copy_(to_dev(base))
+        self.cur.is_flush.copy_(to_dev(flag))
+        self.slot_dev = to_dev(self.slot_idx)
+        self.A_log_dev = to_dev(self.A_log)
+        self.dt_bias_dev = to_dev(self.dt_bias)
+        self.last_errors: dict = {}
+
+    # ------------------------------------------------------------ set-up helpers
+
+    def _token_records(self, n_units_rows: int, n: int):
+        d = self.dims
+        st = gen.token_stream(self.rng, n * n_units_rows, d.H, d.HV, d.K, d.V, self.io,
+                              d.per_key_gate)
+        k = st["k"].reshape(n_units_rows, n, d.H, d.K)
+        v = st["v"].reshape(n_units_rows, n, d.HV, d.V)
+        a = st["a"].reshape((n_units_rows, n, d.HV) + ((d.K,) if d.per_key_gate else ()))
+        a = a - np.float32(self.decay_shift)
+        b = st["b"].reshape(n_units_rows, n, d.HV)
+        g, beta = oracle.gate(self.A_log, a, self.dt_bias, b, per_key_gate=d.per_key_gate)
+        return k, v, g, beta
+
+    def _prefix_states(self, used, n):
+        """fp64 recurrence from S = 0 over n prefix tokens for each used slot."""
+        d = self.dims
+        k, v, g, beta = self._token_records(len(used), n)
+        U = len(used) * d.HV
+        hv_idx = np.arange(d.HV)
+        kk = gen.to_f64(k)[:, :, hv_idx // self.G, :].transpose(0, 2, 1, 3).reshape(U, n, d.K)
+        vv = gen.to_f64(v).transpose(0, 2, 1, 3).reshape(U, n, d.V)
+        if d.per_key_gate:
+            gg = g.transpose(0, 2, 1, 3).reshape(U, n, d.K)
+        else:
+            gg = g.transpose(0, 2, 1).reshape(U, n)
+        bb = beta.transpose(0, 2, 1).reshape(U, n)
+        S = oracle.run_batch(d, np.zeros((U, d.V, d.K)), vv, kk, gg, bb, nthreads=NTHREADS)
+        return S.reshape(len(used), d.HV, d.V, d.K)
+
+    def _fill_history(self, ring, used, wp, base):
+        """Committed history records at (base + o) & (L-1), o < write_pos."""
+        d = self.dims
+        n = d.L
+        k, v, g, beta = self._token_records(len(used), n)
+        for i, slot in enumerate(used):
+            for o in range(int(wp[slot])):
+                p = (int(base[slot]) + o) & (d.L - 1)
+                ring["rawk"][slot, :, p] = k[i, o]
+                ring["rawv"][slot, :, p] = v[i, o]
+                ring["g"][slot, :, p] = g[i, o].astype(np.float32)
+                ring["beta"][slot, :, p] = beta[i, o].astype(np.float32)
+
+    # ------------------------------------------------------------ one round
+
+    def window(self):
+        d = self.dims
+        w = gen.window_inputs(self.rng, self.B, d.T, d.H, d.HV, d.K, d.V, self.io, d.per_key_gate)
+        if self.decay_shift:
+            a = gen.to_f64(w["a"]).astype(np.float32) - np.float32(self.decay_shift)
+            w["a"] = gen.store(a, self.io)
+        return w
+
+    def verify(self, w, unit_mask=None, run_oracle=True):
+        dev = {name: to_dev(x) for name, x in w.items()}
+        out = binding.verify(self.layer, self.cur, self.slot_dev, dev["q"], dev["k"], dev["v"],
+                             dev["a"], dev["b"], self.A_log_dev, self.dt_bias_dev)
+        o_orc = st = None
+        if run_oracle:
+            f = {name: gen.to_f64(x) for name, x in w.items()}
+            o_orc, st = oracle.verify(self.dims, self.orc, self.orc_cur, self.slot_idx, f["q"],
+                                      f["k"], f["v"], f["a"], f["b"], self.A_log, self.dt_bias,
+                                      unit_mask=unit_mask, nthreads=NTHREADS)
+        return out, o_orc, st
+
+    def commit(self, acc: np.ndarray):
+        binding.commit(self.cur, self.dims.T, self.dims.L, self.slot_dev, to_dev(acc))
+        return oracle.commit(self.dims, self.orc_cur, self.slot_idx, acc)
+
+    def fold(self):
+        binding.fold(self.layer, self.cur, self.slot_dev)
+        return oracle.fold(self.dims, self.orc, self.orc_cur, self.slot_idx, nthreads=NTHREADS)
+
+    # ------------------------------------------------------------ comparisons
+
+    def out_error(self, out_dev, o_orc, rows=None) -> float:
+        got = gen.to_f64(to_host(out_dev))
+        if rows is not None:
+            got, o_orc = got[rows], o_orc[rows]
+        return float(np.max(np.abs(got - o_orc))) if got.size else 0.0
+
+    def check_cursors(self):
+        for name in ("write_pos", "cache_base", "is_flush"):
+            got = to_host(getattr(self.cur, name))
+            want = getattr(self.orc_cur, name)
+            assert np.array_equal(got, want), (name, got, want)
+
+    def check_ring(self):
+        """rawv/rawk bitwise (via exact fp64 values), g/beta within GATE_TOL, and
+        every position the oracle left alone still equal to the template."""
+        rv, rk = gen.to_f64(to_host(self.layer.rawv)), gen.to_f64(to_host(self.layer.rawk))
+        assert np.array_equal(rv, self.orc.rawv), "rawv differs"
+        assert np.array_equal(rk, self.orc.rawk), "rawk differs"
+        g = to_host(self.layer.ring_g).astype(np.float64)
+        be = to_host(self.layer.ring_beta).astype(np.float64)
+        err_g = float(np.max(np.abs(g - self.orc.ring_g)))
+        err_b = float(np.max(np.abs(be - self.orc.ring_beta)))
+        assert err_g <= GATE_TOL and err_b <= GATE_TOL, (err_g, err_b)
+        untouched_g = self.orc.ring_g == self.ring0["g"].astype(np.float64)
+        assert np.array_equal(g[untouched_g], self.orc.ring_g[untouched_g])
+        self.last_errors.update(ring_g=err_g, ring_beta=err_b)
+
+    def ckpt_error(self, slots=None) -> float:
+        got = to_host(self.layer.checkpoint).astype(np.float64)
+        want = self.orc.checkpoint
+        if slots is not None:
+            got, want = got[slots], want[slots]
+        den = np.linalg.norm(want)
+        return float(np.linalg.norm(got - want) / den) if den > 0 else float(np.linalg.norm(got))
+
+    def out_tol(self) -> float:
+        return OUT_TOL_BF16 if self.io == gen.BF16 else OUT_TOL_FP32
