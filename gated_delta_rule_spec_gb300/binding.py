@@ -21,7 +21,7 @@ from . import build as _build
 
 GATE_SCALAR, GATE_PER_KEY = 0, 1
 DTYPE_BF16, DTYPE_FP32 = 0, 1
-ST_ACCEPT_RANGE, ST_SLOT_OOR, ST_RING_OVERFLOW, ST_CURSOR_CORRUPT = 1, 2, 4, 8
+ST_ACCEPT_RANGE, ST_SLOT_OOR, ST_RING_OVERFLOW, ST_CURSOR_CORRUPT, ST_TIMEOUT = 1, 2, 4, 8, 16
 
 _IO_TORCH = {DTYPE_BF16: torch.bfloat16, DTYPE_FP32: torch.float32}
 _NAME_TO_DTYPE = {"bf16": DTYPE_BF16, "fp32": DTYPE_FP32}

@@ -63,6 +63,7 @@ def test_python_constants_match_header():
     assert d["GDN_SPEC_ST_SLOT_OOR"] == binding.ST_SLOT_OOR
     assert d["GDN_SPEC_ST_RING_OVERFLOW"] == binding.ST_RING_OVERFLOW
     assert d["GDN_SPEC_ST_CURSOR_CORRUPT"] == binding.ST_CURSOR_CORRUPT
+    assert d["GDN_SPEC_ST_TIMEOUT"] == binding.ST_TIMEOUT
 
 
 def test_descriptor_layout_matches_header():

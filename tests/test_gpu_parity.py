@@ -61,6 +61,7 @@ def test_c0_shape_bf16_many_rounds(decay_shift):
 def test_c1_qwen3next_b1_200_rounds(record_property):
     wl = WL["C1"]
     sc = Scenario(wl, B=1, seed=0)
+    assert binding.verify_path(sc.layer) == "tc"
     worst = _rounds(sc, wl.rounds, check_ring_every=10)
     record_property("bf16_out_max_abs_err", worst["out"])
     print(f"C1: max-abs output error {worst['out']:.3e}, checkpoint rel-Fro {worst['ckpt']:.3e}")
@@ -72,6 +73,15 @@ def test_c1_weak_decay_heads():
     wl = WL["C1"]
     sc = Scenario(wl, B=2, seed=3, decay_shift=4.0, prefix=32)
     _rounds(sc, 40, full_frac=0.5, check_ring_every=5)
+
+
+def test_qwen3next_shape_generic_kernel_l128():
+    """The CUDA-core kernel at the Qwen3-Next head shape (a 128-record ring is
+    outside the tensor-core kernel's range, so this layer takes the generic one)."""
+    wl = gen.Workload("qwen3next-l128", B=3, H=16, HV=32, K=128, V=128, T=4, L=128, prefix=32)
+    sc = Scenario(wl, B=3, seed=12, num_slots=5, random_cursors=True)
+    assert binding.verify_path(sc.layer) == "generic"
+    _rounds(sc, 12, check_ring_every=3)
 
 
 @pytest.mark.parametrize("B", [8, 32, 128, 256])
