@@ -12,8 +12,9 @@
 //              T window queries (rows 64..64+T-1 of X), K = 128 contraction
 //              -> tcgen05.mma kind::tf32, fp32 accumulator in TMEM.
 //   per row i  A[i, r] = beta_i Gamma(i, r) G[i, r], F[i, s] = Gamma(W+s, i) G[i, 64+s]
-//              (decays as running products of alpha; one thread per token)
-//   M          M (I + A) = F^T, backward substitution (one warp per window token)
+//              (one thread per token; decays are products of alpha, never
+//              exponentials of differences of long sums)
+//   M          M (I + A) = F^T, backward substitution, one warp for all T rows
 //   q_eff_s    eG_{W+s} q^_s - sum_j M[s, j] beta_j eG_j k^_j       (K-vector)
 //   P          P = S0 q_eff^T: the checkpoint tile times T columns
 //              -> tcgen05.mma kind::tf32 with S0 staged by TMA.
@@ -22,12 +23,12 @@
 // path; everything else is O(n) per thread or O(n^2) per CTA on CUDA cores.
 //
 // Data movement: the checkpoint tile (128 x 128 fp32 = 64 KiB) is the bulk of
-// the bytes.  Its L2 prefetch is issued as soon as the cursors are known; the
-// keys, gates and ring history are read while it is in flight; the TMA tile
+// the bytes.  Its L2 prefetch is issued as soon as the cursors are known, as
+// is the prefetch of the ring's v history; every other global read of the CTA
+// (keys, queries, gates, window values) is issued in one round.  The TMA tile
 // load into shared memory is issued after the key buffers are dead, so the
-// checkpoint tile reuses their space and the CTA needs ~77 KiB of shared
-// memory (two CTAs per SM).  The ring history of v is prefetched to L2 too and
-// read by each thread for its own row.
+// tile reuses their space and the CTA needs ~73 KiB of shared memory: three
+// CTAs per SM.
 //
 // Side channel (sglang PR #36821 ring-write placement): the window's raw k
 // (one writer per k-head), raw v (each V-block its rows) and the fp32 g and
@@ -51,29 +52,34 @@ constexpr int kXRows = 80;         // Gram N (keys + queries, padded to 16)
 constexpr int kXAtom = kXRows * 128;   // bytes of one 32-float K slice of X
 constexpr int kS0Atom = kBV * 128;     // bytes of one 32-float K slice of S0
 constexpr int kQAtom = 16 * 128;       // bytes of one K slice of q_eff (N = 16)
-constexpr int kALd = kLMax + 1;        // row stride (floats) of A
-constexpr int kFLd = kLMax;            // row stride (floats) of F and c
+constexpr int kALd = kLMax;            // row stride (floats) of A (zero above the diagonal)
 
-// shared-memory map (bytes from a 1024-aligned base); R0 is reused: first the
-// key phase (X, A, F, gates), then the checkpoint tile
+// Shared-memory map (bytes from a 1024-aligned base).  R0 holds first the key
+// phase (X, A, F, gates, decay products), then the checkpoint tile.  R1 is
+// the q_eff operand of the second MMA (16 rows of 128 fp32); rows 8..15 of
+// its first two K slices, which only feed output columns that are never read,
+// hold c = M beta for the output.
 constexpr int kOffX = 0;
-constexpr int kOffA = kOffX + 4 * kXAtom;                    // 40960
-constexpr int kOffF = kOffA + kLMax * kALd * 4;              // 57600
-constexpr int kOffAlpha = kOffF + kTMax * kFLd * 4;          // 59648
+constexpr int kOffA = kOffX + 4 * kXAtom;                     // 40960
+constexpr int kOffF = kOffA + kLMax * kALd * 4;               // 57344: F, then c eG
+constexpr int kOffAlpha = kOffF + kLMax * kTMax * 4;          // 59392
 constexpr int kOffBeta = kOffAlpha + kLMax * 4;
 constexpr int kOffEG = kOffBeta + kLMax * 4;
-constexpr int kEndKeyPhase = kOffEG + kLMax * 4;             // 60416
+constexpr int kOffSuf = kOffEG + kLMax * 4;                   // suffix products, L+1 floats
+constexpr int kOffWP = kOffSuf + (kLMax + 4) * 4;             // window products
+constexpr int kEndKeyPhase = kOffWP + kTMax * 4;
 constexpr int kOffS0 = 0;
-constexpr int kR0Bytes = 4 * kS0Atom;                        // 65536
-constexpr int kOffQ = kR0Bytes;                              // q_eff operand
-constexpr int kOffC = kOffQ + 4 * kQAtom;                    // 73728: c = M beta
-constexpr int kOffBar = kOffC + kTMax * kFLd * 4;            // 75776
+constexpr int kR0Bytes = 4 * kS0Atom;                         // 65536
+constexpr int kOffQ = kR0Bytes;                               // q_eff operand, 8 KiB
+constexpr int kOffBar = kOffQ + 4 * kQAtom;                   // 73728
 constexpr int kOffMisc = kOffBar + 32;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;             // + alignment slack
+constexpr int kSmemUsed = kOffMisc + 32;
+constexpr int kSmemBytes = kSmemUsed + 1024;                  // + alignment slack
 static_assert(kEndKeyPhase <= kR0Bytes, "key phase must fit under the checkpoint tile");
 // the Gram's A operand reads 128 rows of each X slice; slice 3 runs 48 rows
 // past X into the A matrix, which is inside shared memory
 static_assert(3 * kXAtom + 128 * 128 <= kR0Bytes, "Gram operand overrun leaves R0");
+static_assert(3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
 
 constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kGramCol = 0;
@@ -85,7 +91,23 @@ __device__ __forceinline__ uint32_t sw128(int atom_bytes, int row, int k) {
     return atom * atom_bytes + row * 128 + (((chunk ^ (row & 7)) << 4) | (byte & 15));
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+// c[j][s] (j < 64, s < 8) in rows 8..15 of the q_eff operand's first two K slices
+__device__ __forceinline__ uint32_t c_off(int j) {
+    return kOffQ + (j >> 5) * kQAtom + 1024 + (j & 31) * 32;
+}
+
+// warp-wide inclusive prefix product of x
+__device__ __forceinline__ float warp_prefix_prod(float x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x *= y;
+    }
+    return x;
+}
+
+template <int TM>
+__global__ void __launch_bounds__(kThreads, 3)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, CursorArgs C,
                  const int32_t *__restrict__ slot_idx, const __nv_bfloat16 *__restrict__ q,
                  const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
@@ -98,11 +120,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
     uint8_t *sm = smem_raw + pad;
     const uint32_t sm_s = raw_s + pad;
     float *A = reinterpret_cast<float *>(sm + kOffA);
-    float *F = reinterpret_cast<float *>(sm + kOffF);
+    float *F = reinterpret_cast<float *>(sm + kOffF);         // F[j][s], later c eG [j][s]
     float *alpha = reinterpret_cast<float *>(sm + kOffAlpha);
     float *betaS = reinterpret_cast<float *>(sm + kOffBeta);
     float *eG = reinterpret_cast<float *>(sm + kOffEG);
-    float *cm = reinterpret_cast<float *>(sm + kOffC);
+    float *suf = reinterpret_cast<float *>(sm + kOffSuf);
+    float *wprod = reinterpret_cast<float *>(sm + kOffWP);
     int *misc = reinterpret_cast<int *>(sm + kOffMisc);  // slot, base, W, ok, tmem, err
     const uint32_t bar_gram = sm_s + kOffBar, bar_s0 = sm_s + kOffBar + 8,
                    bar_p = sm_s + kOffBar + 16;
@@ -139,7 +162,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         }
     }
     if (warp == 0) ptx::tmem_alloc(sm_s + kOffMisc + 16, kTmemCols);
-    // zero the q_eff operand (rows T..15 stay zero)
+    // zero the q_eff operand: rows T..7 must be zero-or-ignored, rows 8..15 get c
     for (int i = tid; i < 4 * kQAtom / 16; i += kThreads)
         reinterpret_cast<float4 *>(sm + kOffQ)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     ptx::tc_fence_before_sync();
@@ -159,79 +182,83 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         __nv_bfloat16 *rawv_w = reinterpret_cast<__nv_bfloat16 *>(P.rawv);
         const bool k_writer = (hv % P.G == 0) && vb == 0;
 
-        // ---- 1. keys (rows 0..n-1) and queries (rows 64..64+T-1): load, L2-normalise,
-        //         store fp32 into X in the SW128 K-major layout.  Lane l holds k = 4l..4l+3.
-        {
-            constexpr int kRowsPerWarp = (kLMax + kTMax) / 4;  // 18
-            uint2 raw[kRowsPerWarp];
+        // ---- 1. one round of global reads: keys (rows 0..n-1), queries (rows
+        //         64..), gate inputs of token tid, window values of row tid
+        constexpr int kRowsPerWarp = (kLMax + kTMax) / 4;  // 18
+        uint2 raw[kRowsPerWarp];
 #pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const int t = warp + 4 * i;  // token index: keys 0..n-1, then queries
-                raw[i] = make_uint2(0u, 0u);
-                if (t < n + T) {
-                    const __nv_bfloat16 *src;
-                    if (t < W)
-                        src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
-                    else if (t < n)
-                        src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
-                    else
-                        src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
-                    raw[i] = reinterpret_cast<const uint2 *>(src)[lane];
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kRowsPerWarp; ++i) {
-                const int t = warp + 4 * i;
-                if (t < n + T) {
-                    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i].x);
-                    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i].y);
-                    const float2 f0 = __bfloat1622float2(lo), f1 = __bfloat1622float2(hi);
-                    float ss = f0.x * f0.x + f0.y * f0.y + f1.x * f1.x + f1.y * f1.y;
-                    ss = warp_sum(ss);
-                    const float r = 1.0f / sqrtf(ss + P.l2_eps);
-                    const int row = t < n ? t : kQRow + (t - n);
-                    *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, 4 * lane)) =
-                        make_float4(f0.x * r, f0.y * r, f1.x * r, f1.y * r);
-                    if (t >= W && t < n && k_writer)  // side channel: raw key, bitwise
-                        reinterpret_cast<uint2 *>(rawk_w + (sh_h * L + ring_pos(base, t, L)) * kK)[lane] =
-                            raw[i];
-                }
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int t = warp + 4 * i;  // token index: keys 0..n-1, then queries
+            raw[i] = make_uint2(0u, 0u);
+            if (t < n + T) {
+                const __nv_bfloat16 *src;
+                if (t < W)
+                    src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
+                else if (t < n)
+                    src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
+                else
+                    src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
+                raw[i] = reinterpret_cast<const uint2 *>(src)[lane];
             }
         }
-        // ---- 2. gates: history from the ring, window computed (and written to the ring)
+        float g_in = 0.f, b_in = 0.f, alog = 0.f, dtb = 0.f;
+        const int pj = ring_pos(base, tid, L);
+        if (tid < W) {
+            g_in = P.ring_g[sh_hv * L + pj];
+            b_in = P.ring_beta[sh_hv * L + pj];
+        } else if (tid < n) {
+            const size_t tok = (size_t)bb * T + (tid - W);
+            g_in = __bfloat162float(a[tok * HV + hv]);
+            b_in = __bfloat162float(bgate[tok * HV + hv]);
+            alog = A_log[hv];
+            dtb = dt_bias[hv];
+        }
+        __nv_bfloat16 vwin_raw[TM];
+#pragma unroll
+        for (int s = 0; s < TM; ++s)
+            vwin_raw[s] = (s < T && vrow < V) ? v[(((size_t)bb * T + s) * HV + hv) * V + vrow]
+                                               : __float2bfloat16_rn(0.0f);
+
+        // normalise into X (SW128 K-major), ring side channel for the window keys
+#pragma unroll
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int t = warp + 4 * i;
+            if (t < n + T) {
+                const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i].x);
+                const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i].y);
+                const float2 f0 = __bfloat1622float2(lo), f1 = __bfloat1622float2(hi);
+                float ss = f0.x * f0.x + f0.y * f0.y + f1.x * f1.x + f1.y * f1.y;
+                ss = warp_sum(ss);
+                const float r = 1.0f / sqrtf(ss + P.l2_eps);
+                const int row = t < n ? t : kQRow + (t - n);
+                *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, 4 * lane)) =
+                    make_float4(f0.x * r, f0.y * r, f1.x * r, f1.y * r);
+                if (t >= W && t < n && k_writer)
+                    reinterpret_cast<uint2 *>(rawk_w + (sh_h * L + ring_pos(base, t, L)) * kK)[lane] =
+                        raw[i];
+            }
+        }
         if (tid < n) {
-            const int j = tid, p = ring_pos(base, j, L);
-            float g, be;
-            if (j < W) {
-                g = P.ring_g[sh_hv * L + p];
-                be = P.ring_beta[sh_hv * L + p];
-            } else {
-                const size_t tok = (size_t)bb * T + (j - W);
-                g = gate_g(A_log[hv], __bfloat162float(a[tok * HV + hv]), dt_bias[hv]);
-                be = gate_beta(__bfloat162float(bgate[tok * HV + hv]));
+            float g = g_in, be = b_in;
+            if (tid >= W) {
+                g = gate_g(alog, g_in, dtb);
+                be = gate_beta(b_in);
                 if (vb == 0) {
-                    P.ring_g[sh_hv * L + p] = g;
-                    P.ring_beta[sh_hv * L + p] = be;
+                    P.ring_g[sh_hv * L + pj] = g;
+                    P.ring_beta[sh_hv * L + pj] = be;
                 }
             }
-            alpha[j] = expf(g);
-            betaS[j] = be;
+            alpha[tid] = expf(g);
+            betaS[tid] = be;
         }
-        // window values of this thread's row: kept for the output, copied to the ring
-        float vwin[kTMax];
 #pragma unroll
-        for (int s = 0; s < kTMax; ++s) {
-            vwin[s] = 0.0f;
-            if (s < T && vrow < V) {
-                const __nv_bfloat16 x = v[(((size_t)bb * T + s) * HV + hv) * V + vrow];
-                rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = x;
-                vwin[s] = __bfloat162float(x);
-            }
-        }
+        for (int s = 0; s < TM; ++s)
+            if (s < T && vrow < V) rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = vwin_raw[s];
         ptx::fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- 3. Gram on the tensor core: D[i, j] = <X_i, X_j>, M = 128, N = 80
+        // ---- 2. Gram on the tensor core (D[i, j] = <X_i, X_j>, M = 128, N = 80),
+        //         decay products on CUDA cores meanwhile
         if (tid == 0) {
             ptx::tc_fence_after_sync();
             constexpr uint32_t idesc = ptx::idesc_tf32(128, kXRows);
@@ -244,89 +271,175 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 }
             ptx::mma_commit(bar_gram);
         }
+        if (warp == 1) {  // eG_j = prod_{t <= j} alpha_t, j < n
+            const float a0 = 2 * lane < n ? alpha[2 * lane] : 1.0f;
+            const float a1 = 2 * lane + 1 < n ? alpha[2 * lane + 1] : 1.0f;
+            const float incl = warp_prefix_prod(a0 * a1, lane);
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane == 0) excl = 1.0f;
+            eG[2 * lane] = excl * a0;
+            eG[2 * lane + 1] = incl;
+        } else if (warp == 2) {  // suf[t] = prod_{u=t}^{W-1} alpha_u, t <= W (suf[W] = 1)
+            const int u0 = 2 * lane, u1 = 2 * lane + 1;  // reversed index u = W-1-t
+            const float a0 = u0 < W ? alpha[W - 1 - u0] : 1.0f;
+            const float a1 = u1 < W ? alpha[W - 1 - u1] : 1.0f;
+            const float incl = warp_prefix_prod(a0 * a1, lane);
+            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+            if (lane == 0) excl = 1.0f;
+            if (u0 < W) suf[W - 1 - u0] = excl * a0;
+            if (u1 < W) suf[W - 1 - u1] = incl;
+            if (lane == 0) suf[W] = 1.0f;
+        } else if (warp == 3 && lane == 0) {  // wprod[s] = prod_{t=W}^{W+s} alpha_t
+            float c = 1.0f;
+#pragma unroll
+            for (int s = 0; s < TM; ++s)
+                if (s < T) {
+                    c *= alpha[W + s];
+                    wprod[s] = c;
+                }
+        }
+        __syncthreads();
         bool waited = ptx::mbar_wait(bar_gram, 0);
         ptx::tc_fence_after_sync();
-        float g[kXRows];
+
+        // ---- 3. per token i (thread i): row i of A (zero above the diagonal), row i of F
         {
+            const int i = tid;
             const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + kGramCol;
+            float gq[16];
+            ptx::tmem_ld16(tbase + kQRow, gq);   // columns 64..79: the query columns
+            float gk[64];
 #pragma unroll
-            for (int c = 0; c < kXRows / 16; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 float r[16];
                 ptx::tmem_ld16(tbase + 16 * c, r);
 #pragma unroll
-                for (int x = 0; x < 16; ++x) g[16 * c + x] = r[x];
+                for (int x = 0; x < 16; ++x) gk[16 * c + x] = r[x];
             }
             ptx::tmem_ld_wait();
+            if (i < n) {
+                const float bi = betaS[i];
+                float c = 1.0f;
+#pragma unroll
+                for (int r = kLMax - 1; r >= 0; --r) {
+                    float val = 0.0f;
+                    if (r < i) {
+                        c *= alpha[r + 1];               // Gamma(i, r)
+                        val = bi * c * gk[r];
+                    }
+                    A[i * kALd + r] = val;
+                }
+                // Gamma(W+s, i): products of the suffix and window decays
+                const float si = i < W ? suf[i + 1] : 1.0f;
+                float cw = 1.0f;
+                float fr[TM];
+#pragma unroll
+                for (int s = 0; s < TM; ++s) {
+                    float f = 0.0f;
+                    if (s < T) {
+                        const int t = W + s;
+                        if (i < W) {
+                            f = si * wprod[s] * gq[s];
+                        } else if (t >= i) {
+                            if (t > i) cw *= alpha[t];
+                            f = cw * gq[s];
+                        }
+                    }
+                    fr[s] = f;
+                }
+#pragma unroll
+                for (int s = 0; s < TM; s += 4)
+                    *reinterpret_cast<float4 *>(F + i * TM + s) = make_float4(fr[s], fr[s + 1], fr[s + 2], fr[s + 3]);
+            }
         }
         if (!waited && tid == 0) misc[5] = 1;
+        __syncthreads();
 
-        // ---- 4. per token i (thread i): row i of A, row i of F, eG_i
-        const int i = tid;
-        if (i < n) {
-            const float bi = betaS[i];
-            float c = 1.0f;
+        // the v history of this thread's row (L2-resident), held for the output
+        // (two bf16 per register)
+        __nv_bfloat162 rv[kLMax / 2];
 #pragma unroll
-            for (int r = kLMax - 1; r >= 0; --r) {
-                if (r < i) {
-                    c *= alpha[r + 1];                       // Gamma(i, r)
-                    A[i * kALd + r] = bi * c * g[r];
+        for (int jp = 0; jp < kLMax / 2; ++jp) {
+            const int j0 = 2 * jp, j1 = 2 * jp + 1;
+            const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
+            const __nv_bfloat16 x0 =
+                (j0 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j0, L)) * V + vrow] : z;
+            const __nv_bfloat16 x1 =
+                (j1 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j1, L)) * V + vrow] : z;
+            rv[jp] = __halves2bfloat162(x0, x1);
+        }
+
+        // ---- 4. M (I + A) = F^T, all T rows in warp 0; lane l ends with M[s][l], M[s][l+32]
+        if (warp == 0) {
+            float f0[TM], f1[TM];
+#pragma unroll
+            for (int s = 0; s < TM; ++s) {
+                f0[s] = lane < n ? F[lane * TM + s] : 0.0f;
+                f1[s] = lane + 32 < n ? F[(lane + 32) * TM + s] : 0.0f;
+            }
+            for (int j = n - 1; j >= 0; --j) {
+                const float a0 = A[j * kALd + lane], a1 = A[j * kALd + 32 + lane];
+#pragma unroll
+                for (int s = 0; s < TM; ++s) {
+                    const float m = __shfl_sync(0xffffffffu, j < 32 ? f0[s] : f1[s], j & 31);
+                    f0[s] = fmaf(-a0, m, f0[s]);
+                    f1[s] = fmaf(-a1, m, f1[s]);
                 }
             }
-            float cf = 1.0f;
-            for (int t = i + 1; t < W; ++t) cf *= alpha[t];  // Gamma(W-1, i)
+            // c = M beta (output) and c eG (effective query), rows j = lane, lane + 32
 #pragma unroll
-            for (int s = 0; s < kTMax; ++s) {
-                if (s < T) {
-                    const int t = W + s;
-                    if (t > i) cf *= alpha[t];
-                    F[s * kFLd + i] = t >= i ? cf * g[kQRow + s] : 0.0f;
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const int j = lane + 32 * hlf;
+                const float bj = j < n ? betaS[j] : 0.0f, ej = j < n ? eG[j] : 0.0f;
+                float cj[TM], ce[TM];
+#pragma unroll
+                for (int s = 0; s < TM; ++s) {
+                    cj[s] = (hlf ? f1[s] : f0[s]) * bj;
+                    ce[s] = cj[s] * ej;
+                }
+#pragma unroll
+                for (int s = 0; s < TM; s += 4) {
+                    *reinterpret_cast<float4 *>(sm + c_off(j) + 4 * s) =
+                        make_float4(cj[s], cj[s + 1], cj[s + 2], cj[s + 3]);
+                    *reinterpret_cast<float4 *>(F + j * TM + s) =
+                        make_float4(ce[s], ce[s + 1], ce[s + 2], ce[s + 3]);
                 }
             }
-            float e = 1.0f;
-            for (int t = 0; t <= i; ++t) e *= alpha[t];
-            eG[i] = e;
         }
         __syncthreads();
 
-        // ---- 5. M (I + A) = F^T by backward substitution; c[s, j] = M[s, j] beta_j
-        for (int s = warp; s < T; s += kThreads / 32) {
-            float f0 = lane < n ? F[s * kFLd + lane] : 0.0f;
-            float f1 = lane + 32 < n ? F[s * kFLd + lane + 32] : 0.0f;
-            for (int j = W + s; j >= 0; --j) {
-                const float m = __shfl_sync(0xffffffffu, j < 32 ? f0 : f1, j & 31);
-                if (lane == 0) cm[s * kFLd + j] = m * betaS[j];
-                if (lane < j) f0 -= A[j * kALd + lane] * m;
-                if (lane + 32 < j) f1 -= A[j * kALd + lane + 32] * m;
-            }
-            for (int j = W + s + 1 + lane; j < kLMax; j += 32) cm[s * kFLd + j] = 0.0f;
-        }
-        __syncthreads();
-
-        // ---- 6. q_eff (thread = key channel): eG_{W+s} q^_s - sum_j c[s, j] eG_j k^_j
+        // ---- 5. q_eff (thread = key channel): eG_{W+s} q^_s - sum_j c[j][s] eG_j k^_j
         {
             const int kk = tid;
-            float acc[kTMax];
+            const int katom = kk >> 5, kbyte = (kk & 31) * 4, kch = kbyte >> 4;
+            const uint32_t xbase = kOffX + katom * kXAtom + (kbyte & 15);
+            float acc[TM];
 #pragma unroll
-            for (int s = 0; s < kTMax; ++s) acc[s] = 0.0f;
+            for (int s = 0; s < TM; ++s) acc[s] = 0.0f;
             for (int j = 0; j < n; ++j) {
-                const float x = eG[j] * *reinterpret_cast<const float *>(sm + kOffX + sw128(kXAtom, j, kk));
+                const float x = *reinterpret_cast<const float *>(sm + xbase + j * 128 + ((kch ^ (j & 7)) << 4));
 #pragma unroll
-                for (int s = 0; s < kTMax; ++s)
-                    if (s < T) acc[s] -= cm[s * kFLd + j] * x;
-            }
-#pragma unroll
-            for (int s = 0; s < kTMax; ++s) {
-                if (s < T) {
-                    acc[s] += eG[W + s] *
-                              *reinterpret_cast<const float *>(sm + kOffX + sw128(kXAtom, kQRow + s, kk));
-                    *reinterpret_cast<float *>(sm + kOffQ + sw128(kQAtom, s, kk)) = acc[s];
+                for (int s = 0; s < TM; s += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(F + j * TM + s);
+                    acc[s] = fmaf(-c4.x, x, acc[s]);
+                    acc[s + 1] = fmaf(-c4.y, x, acc[s + 1]);
+                    acc[s + 2] = fmaf(-c4.z, x, acc[s + 2]);
+                    acc[s + 3] = fmaf(-c4.w, x, acc[s + 3]);
                 }
             }
+#pragma unroll
+            for (int s = 0; s < TM; ++s)
+                if (s < T)
+                    acc[s] += eG[W + s] * *reinterpret_cast<const float *>(
+                                              sm + xbase + (kQRow + s) * 128 + ((kch ^ ((kQRow + s) & 7)) << 4));
+#pragma unroll
+            for (int s = 0; s < TM; ++s)
+                if (s < T) *reinterpret_cast<float *>(sm + kOffQ + sw128(kQAtom, s, kk)) = acc[s];
         }
         ptx::fence_proxy_async_smem();
         __syncthreads();
 
-        // ---- 7. checkpoint tile by TMA (over the dead key buffers), then P = S0 q_eff^T
+        // ---- 6. checkpoint tile by TMA (over the dead key buffers), then P = S0 q_eff^T
         if (tid == 0) {
             ptx::fence_proxy_async_smem();
             ptx::mbar_expect_tx(bar_s0, kR0Bytes);
@@ -335,28 +448,28 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             for (int kb = 0; kb < 4; ++kb)
                 ptx::tma_load_2d(sm_s + kOffS0 + kb * kS0Atom, &tmap_s0, bar_s0, kb * 32, y);
         }
-        // the v history of this thread's row (L2-resident by now), folded with c
-        float vt[kTMax];
+        // output part that does not need the checkpoint: sum_j c[j][s] v_j
+        float vt[TM];
 #pragma unroll
-        for (int s = 0; s < kTMax; ++s) vt[s] = 0.0f;
-        if (vrow < V) {
-            for (int j0 = 0; j0 < W; j0 += 8) {
-                float x[8];
+        for (int s = 0; s < TM; ++s) vt[s] = 0.0f;
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    x[u] = j0 + u < W ? __bfloat162float(rawv[(sh_hv * L + ring_pos(base, j0 + u, L)) * V + vrow])
-                                      : 0.0f;
+        for (int j = 0; j < kLMax + TM; ++j) {
+            // history records j < W from registers, then the window values
+            const bool hist = j < kLMax;
+            const int jj = hist ? j : W + (j - kLMax);
+            if (hist ? j < W : (j - kLMax) < T) {
+                const float x = hist ? ((j & 1) ? __high2float(rv[hist ? j >> 1 : 0])
+                                                : __low2float(rv[hist ? j >> 1 : 0]))
+                                     : __bfloat162float(vwin_raw[hist ? 0 : j - kLMax]);
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-#pragma unroll
-                    for (int s = 0; s < kTMax; ++s)
-                        if (s < T && j0 + u < W) vt[s] += cm[s * kFLd + j0 + u] * x[u];
+                for (int s = 0; s < TM; s += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(jj) + 4 * s);
+                    vt[s] = fmaf(c4.x, x, vt[s]);
+                    vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
+                    vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
+                    vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
+                }
             }
-#pragma unroll
-            for (int s2 = 0; s2 < kTMax; ++s2)
-#pragma unroll
-                for (int s = 0; s < kTMax; ++s)
-                    if (s < T && s2 < T) vt[s] += cm[s * kFLd + W + s2] * vwin[s2];
         }
         waited = ptx::mbar_wait(bar_s0, 0);
         if (tid == 0) {
@@ -384,7 +497,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         if (!waited) misc[5] = 1;
         if (vrow < V) {
 #pragma unroll
-            for (int s = 0; s < kTMax; ++s)
+            for (int s = 0; s < TM; ++s)
                 if (s < T)
                     out[(((size_t)bb * T + s) * HV + hv) * V + vrow] =
                         __float2bfloat16_rn(P.scale * (pr[s] + vt[s]));
@@ -431,6 +544,24 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+template <int TM>
+cudaError_t launch_tm(const CUtensorMap &tmap, const LayerArgs &P, const CursorArgs &C,
+                      const int32_t *slot_idx, int B, const void *q, const void *k, const void *v,
+                      const void *a, const void *b, const float *A_log, const float *dt_bias,
+                      void *out, cudaStream_t stream) {
+    auto kern = tc::verify_tc_kernel<TM>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tc::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(P.HV, B, P.V / tc::kBV);
+    kern<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(
+        tmap, P, C, slot_idx, static_cast<const __nv_bfloat16 *>(q),
+        static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
+        static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), A_log, dt_bias,
+        static_cast<__nv_bfloat16 *>(out));
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_verify_tc(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
@@ -450,17 +581,9 @@ cudaError_t launch_verify_tc(const LayerArgs &P, const CursorArgs &C, const int3
                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc::verify_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    dim3 grid(P.HV, B, P.V / tc::kBV);
-    tc::verify_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(
-        tmap, P, C, slot_idx, static_cast<const __nv_bfloat16 *>(q),
-        static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
-        static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), A_log, dt_bias,
-        static_cast<__nv_bfloat16 *>(out));
-    return cudaGetLastError();
+    if (P.T <= 4)
+        return launch_tm<4>(tmap, P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, stream);
+    return launch_tm<8>(tmap, P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, stream);
 }
 
 }  // namespace gdnspec
