@@ -60,7 +60,7 @@ int check_layer(const gdn_spec_layer *L) {
     if (!aligned16(L->checkpoint) || !aligned16(L->rawv) || !aligned16(L->rawk) ||
         !aligned16(L->ring_g) || !aligned16(L->ring_beta))
         return GDN_SPEC_EALIGN;
-    if (L->K > 256 || L->T > 16) return GDN_SPEC_EUNSUPPORTED;
+    if ((L->K != 32 && L->K != 64 && L->K != 128) || L->T > 16) return GDN_SPEC_EUNSUPPORTED;
     if (L->L > (L->gate_kind == GDN_SPEC_GATE_PER_KEY ? 64 : 128)) return GDN_SPEC_EUNSUPPORTED;
     return GDN_SPEC_OK;
 }

@@ -8,48 +8,51 @@
 //     S <- exp(g_t) S   (KDA: S diag(exp(g_t)))
 //     d  = beta_t (v_t - S k^_t),   S <- S + d k^_t^T
 // Rows of S are independent under the recurrence (row i only sees v_t[i]),
-// so the work is parallel over V and sequential over the W records.
+// so one thread owns one state row: its K values live in registers, the dot
+// product needs no shuffles, and the records are replayed one after another.
+// The elementwise work uses Blackwell's packed fp32x2 instructions.
 //
 // Only the rows whose is_flush is set do any work, and in steady state that
 // is a small share of the batch per step.  So the grid is persistent: every
 // CTA scans the batch's flags, builds the same compact list of rows to fold,
-// and takes work items (row, layer, v-head, block of 32 state rows)
-// round-robin from it.  For an item, every global read (keys, gates, values)
-// is issued in one round; then four threads per state row hold K/4 state
-// values each in registers and replay the records.  Folding runs after
-// sampling, outside the forward, so the layers are independent here and one
-// launch folds all of them (the blog's §2.1 observation about replay outside
-// the forward).  The cursors move in a separate launch after every layer.
+// and takes work items (row, layer, v-head, block of 128 state rows)
+// round-robin from it.  For an item every global read (keys, gates, values,
+// the state rows) is issued in one round.  Folding runs after sampling,
+// outside the forward, so the layers are independent here and one launch
+// folds all of them (the blog's §2.1 observation about replay outside the
+// forward).  The cursors move in a separate launch after every layer.
 #include "common.cuh"
 
 namespace gdnspec {
 
 constexpr int kFoldThreads = 128;
-constexpr int kFoldRows = kFoldThreads / 4;  // state rows per work item
-constexpr int kFoldMaxL = 128;               // ring length limit of this kernel
-constexpr int kFoldScan = kFoldThreads;      // batch rows scanned per pass
+constexpr int kFoldMaxL = 128;   // ring length limit of this kernel
+constexpr int kFoldScan = kFoldThreads;
 
+// Shared memory of one item: raw keys [L][K] fp32, alpha [L] (KDA [L][K]),
+// beta [L], 1/|k| [L], values [L][128 rows] fp32, and the compacted row list.
 size_t fold_smem_bytes(int K, int L, bool kda) {
-    // keys [L][K], alpha [L] or [L][K], beta [L], values [L][kFoldRows], row list
-    return sizeof(float) * ((size_t)L * K + (size_t)L * (kda ? K : 1) + L + (size_t)L * kFoldRows) +
+    return sizeof(float) * ((size_t)L * K + (size_t)L * (kda ? K : 1) + 2 * L + (size_t)L * kFoldThreads) +
            sizeof(int) * 2 * kFoldScan;
 }
 
-template <typename IO, bool KDA, int KC>
-__global__ void __launch_bounds__(kFoldThreads)
+template <typename IO, bool KDA, int K>
+__global__ void __launch_bounds__(kFoldThreads, 2)
 fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int32_t *__restrict__ slot_idx, int B) {
+    static_assert(K % 8 == 0 && K <= 128, "one state row per thread");
     extern __shared__ __align__(16) float sm[];
     __shared__ int s_count, s_warp_off[kFoldThreads / 32];
-    const int K = P.K, V = P.V, L = P.L, HV = P.HV, H = P.H;
+    const int V = P.V, L = P.L, HV = P.HV, H = P.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *Xs = sm;                                  // [L][K]
     float *alpha = Xs + (size_t)L * K;               // [L] or [L][K]
     float *betaS = alpha + (size_t)L * (KDA ? K : 1);
-    float *vv = betaS + L;                           // [L][kFoldRows]
-    int *rows = reinterpret_cast<int *>(vv + (size_t)L * kFoldRows);  // [kFoldScan] row, [kFoldScan] W|base
+    float *rsS = betaS + L;                          // [L] 1 / |k_t|
+    float *vv = rsS + L;                             // [L][kFoldThreads]
+    int *rows = reinterpret_cast<int *>(vv + (size_t)L * kFoldThreads);
     int *meta = rows + kFoldScan;
-    const int vblocks = (V + kFoldRows - 1) / kFoldRows;
+    const int vblocks = (V + kFoldThreads - 1) / kFoldThreads;
     const int per_row = n_layers * HV * vblocks;
     long long item_base = 0;  // items enumerated in earlier scan passes
 
@@ -98,7 +101,8 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int h = hv / P.G;
             const int slot = slot_idx[rows[e]];
             const int W = meta[e] >> 16, base = meta[e] & 0xFFFF;
-            const int v0 = vbk * kFoldRows;
+            const int vr = vbk * kFoldThreads + tid;   // this thread's state row
+            const bool valid = vr < V;
             const size_t sh_hv = (size_t)slot * HV + hv, sh_h = (size_t)slot * H + h;
             const IO *rawk = reinterpret_cast<const IO *>(FL.rawk[li]);
             const IO *rawv = reinterpret_cast<const IO *>(FL.rawv[li]);
@@ -106,38 +110,53 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const float *ring_beta = FL.ring_beta[li];
             float *ckpt = FL.checkpoint[li];
 
-            // one round of reads: keys (warp-per-record), gates, values
-            constexpr int kRecPerWarp = kFoldMaxL / (kFoldThreads / 32);  // 32
-            constexpr int KPL = KC / 2;  // key elements per lane per record (K / 32)
-            for (int j0 = 0; j0 < W; j0 += kRecPerWarp * (kFoldThreads / 32) / 4) {
-                // records j0 + warp + 4 i, i < 8: keys loaded together, then normalised
-                float kx[8][KPL];
+            // ---- one round of reads: the state row, keys (two threads per
+            //      record), gates (thread per record), values (thread per row)
+            float2 S2[K / 2];
+            const float4 *srow = reinterpret_cast<const float4 *>(ckpt + (sh_hv * V + (valid ? vr : 0)) * K);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = j0 + warp + 4 * i;
+            for (int c = 0; c < K / 4; ++c) {
+                const float4 t4 = valid ? srow[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                S2[2 * c] = make_float2(t4.x, t4.y);
+                S2[2 * c + 1] = make_float2(t4.z, t4.w);
+            }
+            // keys stay raw in shared memory; rs[t] = 1 / |k_t| (with eps) is
+            // applied in the replay, so no key slice is held in registers
+            for (int pass = 0; pass * (kFoldThreads / 2) < W; ++pass) {
+                const int j = pass * (kFoldThreads / 2) + (tid >> 1), half = tid & 1;
+                constexpr int KH = K / 2;   // elements per thread
+                constexpr int kPer = 16 / (int)sizeof(IO);
+                float ss = 0.0f;
+                if (j < W) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        rawk + (sh_h * L + ring_pos(base, j, L)) * K + half * KH);
 #pragma unroll
-                    for (int m = 0; m < KPL; ++m) kx[i][m] = 0.0f;
-                    if (j < W) {
-                        const IO *src = rawk + (sh_h * L + ring_pos(base, j, L)) * K;
+                    for (int c = 0; c < KH / kPer; ++c) {
+                        float x[kPer];
+                        const uint4 u4 = src[c];
+                        if constexpr (sizeof(IO) == 2) {
+                            const uint32_t w[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-                        for (int m = 0; m < KPL; ++m)
-                            if (lane + 32 * m < K) kx[i][m] = to_f32<IO>(src[lane + 32 * m]);
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
+                                x[2 * e] = f.x;
+                                x[2 * e + 1] = f.y;
+                            }
+                        } else {
+                            x[0] = __uint_as_float(u4.x); x[1] = __uint_as_float(u4.y);
+                            x[2] = __uint_as_float(u4.z); x[3] = __uint_as_float(u4.w);
+                        }
+#pragma unroll
+                        for (int e = 0; e < kPer; e += 4) {
+                            ss = fmaf(x[e], x[e], ss); ss = fmaf(x[e + 1], x[e + 1], ss);
+                            ss = fmaf(x[e + 2], x[e + 2], ss); ss = fmaf(x[e + 3], x[e + 3], ss);
+                            *reinterpret_cast<float4 *>(Xs + j * K + half * KH + c * kPer + e) =
+                                make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                        }
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = j0 + warp + 4 * i;
-                    float ss = 0.0f;
-#pragma unroll
-                    for (int m = 0; m < KPL; ++m) ss += kx[i][m] * kx[i][m];
-                    ss = warp_sum(ss);
-                    const float r = 1.0f / sqrtf(ss + P.l2_eps);
-                    if (j < W) {
-#pragma unroll
-                        for (int m = 0; m < KPL; ++m)
-                            if (lane + 32 * m < K) Xs[j * K + lane + 32 * m] = kx[i][m] * r;
-                    }
-                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (j < W && half == 0) rsS[j] = 1.0f / sqrtf(ss + P.l2_eps);
             }
             if (KDA) {
                 for (int idx = tid; idx < W * K; idx += kFoldThreads) {
@@ -150,86 +169,66 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             }
             for (int j = tid; j < W; j += kFoldThreads)
                 betaS[j] = ring_beta[sh_hv * L + ring_pos(base, j, L)];
-            {
-                const int r = tid & (kFoldRows - 1), jq = tid / kFoldRows;  // 4 record lanes
-                const int vr = v0 + r;
-                constexpr int kVals = kFoldMaxL / (kFoldThreads / kFoldRows);  // 32
-                float x[kVals];
+            for (int j0 = 0; j0 < W; j0 += 16) {
+                float xv[16];
 #pragma unroll
-                for (int i = 0; i < kVals; ++i) {
-                    const int j = jq + 4 * i;
-                    x[i] = (j < W && vr < V)
-                               ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vr])
-                               : 0.0f;
-                }
+                for (int u = 0; u < 16; ++u)
+                    xv[u] = (j0 + u < W && valid)
+                                ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j0 + u, L)) * V + vr])
+                                : 0.0f;
 #pragma unroll
-                for (int i = 0; i < kVals; ++i) {
-                    const int j = jq + 4 * i;
-                    if (j < W) vv[j * kFoldRows + r] = x[i];
-                }
+                for (int u = 0; u < 16; ++u)
+                    if (j0 + u < W) vv[(j0 + u) * kFoldThreads + tid] = xv[u];
             }
             __syncthreads();
 
-            // replay: thread (row r, part) holds state columns 4 (part + 4 m) .. + 3
-            const int r = tid >> 2, part = tid & 3;
-            const int vr = v0 + r;
-            const bool valid = vr < V;
-            const int K4 = K / 4;
-            float4 S[KC];
-            float4 *row = reinterpret_cast<float4 *>(ckpt + (sh_hv * V + (valid ? vr : 0)) * K);
-#pragma unroll
-            for (int m = 0; m < KC; ++m) {
-                const int c4 = part + 4 * m;
-                S[m] = (valid && c4 < K4) ? row[c4] : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            // ---- replay (decay, then the delta against the decayed state)
             for (int t = 0; t < W; ++t) {
                 const float4 *xk = reinterpret_cast<const float4 *>(Xs + t * K);
-                float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 if (KDA) {
                     const float4 *al = reinterpret_cast<const float4 *>(alpha + (size_t)t * K);
 #pragma unroll
-                    for (int m = 0; m < KC; ++m) {
-                        const int c4 = part + 4 * m;
-                        if (c4 < K4) {
-                            const float4 a4 = al[c4], x4 = xk[c4];
-                            S[m].x *= a4.x; S[m].y *= a4.y; S[m].z *= a4.z; S[m].w *= a4.w;
-                            u4.x = fmaf(S[m].x, x4.x, u4.x); u4.y = fmaf(S[m].y, x4.y, u4.y);
-                            u4.z = fmaf(S[m].z, x4.z, u4.z); u4.w = fmaf(S[m].w, x4.w, u4.w);
-                        }
+                    for (int c = 0; c < K / 4; ++c) {
+                        const float4 a4 = al[c], x4 = xk[c];
+                        S2[2 * c] = __fmul2_rn(S2[2 * c], make_float2(a4.x, a4.y));
+                        S2[2 * c + 1] = __fmul2_rn(S2[2 * c + 1], make_float2(a4.z, a4.w));
+                        acc[c & 3] = __ffma2_rn(S2[2 * c], make_float2(x4.x, x4.y), acc[c & 3]);
+                        acc[c & 3] = __ffma2_rn(S2[2 * c + 1], make_float2(x4.z, x4.w), acc[c & 3]);
                     }
                 } else {
-                    const float al = alpha[t];
+                    const float a = alpha[t];
+                    const float2 a2 = make_float2(a, a);
 #pragma unroll
-                    for (int m = 0; m < KC; ++m) {
-                        const int c4 = part + 4 * m;
-                        if (c4 < K4) {
-                            const float4 x4 = xk[c4];
-                            S[m].x *= al; S[m].y *= al; S[m].z *= al; S[m].w *= al;
-                            u4.x = fmaf(S[m].x, x4.x, u4.x); u4.y = fmaf(S[m].y, x4.y, u4.y);
-                            u4.z = fmaf(S[m].z, x4.z, u4.z); u4.w = fmaf(S[m].w, x4.w, u4.w);
-                        }
+                    for (int c = 0; c < K / 4; ++c) {
+                        const float4 x4 = xk[c];
+                        S2[2 * c] = __fmul2_rn(S2[2 * c], a2);
+                        S2[2 * c + 1] = __fmul2_rn(S2[2 * c + 1], a2);
+                        acc[c & 3] = __ffma2_rn(S2[2 * c], make_float2(x4.x, x4.y), acc[c & 3]);
+                        acc[c & 3] = __ffma2_rn(S2[2 * c + 1], make_float2(x4.z, x4.w), acc[c & 3]);
                     }
                 }
-                float u = (u4.x + u4.y) + (u4.z + u4.w);
-                u += __shfl_xor_sync(0xffffffffu, u, 1);
-                u += __shfl_xor_sync(0xffffffffu, u, 2);
-                const float d = betaS[t] * (vv[t * kFoldRows + r] - u);
+                const float rs = rsS[t];
+                const float u = rs * (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                                      ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y)));
+                const float d = betaS[t] * (vv[t * kFoldThreads + tid] - u) * rs;
+                const float2 d2 = make_float2(d, d);
+                // re-read the key from shared memory below rather than keeping
+                // all K values of it in registers across the dot product
+                asm volatile("" ::: "memory");
 #pragma unroll
-                for (int m = 0; m < KC; ++m) {
-                    const int c4 = part + 4 * m;
-                    if (c4 < K4) {
-                        const float4 x4 = xk[c4];
-                        S[m].x = fmaf(d, x4.x, S[m].x); S[m].y = fmaf(d, x4.y, S[m].y);
-                        S[m].z = fmaf(d, x4.z, S[m].z); S[m].w = fmaf(d, x4.w, S[m].w);
-                    }
+                for (int c = 0; c < K / 4; ++c) {
+                    const float4 x4 = xk[c];
+                    S2[2 * c] = __ffma2_rn(d2, make_float2(x4.x, x4.y), S2[2 * c]);
+                    S2[2 * c + 1] = __ffma2_rn(d2, make_float2(x4.z, x4.w), S2[2 * c + 1]);
                 }
             }
             if (valid) {
+                float4 *dst = reinterpret_cast<float4 *>(ckpt + (sh_hv * V + vr) * K);
 #pragma unroll
-                for (int m = 0; m < KC; ++m) {
-                    const int c4 = part + 4 * m;
-                    if (c4 < K4) row[c4] = S[m];
-                }
+                for (int c = 0; c < K / 4; ++c)
+                    dst[c] = make_float4(S2[2 * c].x, S2[2 * c].y, S2[2 * c + 1].x, S2[2 * c + 1].y);
             }
             __syncthreads();  // the item's buffers are reused by the next item
         }
@@ -238,32 +237,35 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     }
 }
 
-template <typename IO, bool KDA>
-static cudaError_t launch_fold_typed(const LayerArgs &P, const FoldLayers &FL, int n_layers,
-                                     const CursorArgs &C, const int32_t *slot_idx, int B,
-                                     cudaStream_t stream) {
-    const size_t smem = fold_smem_bytes(P.K, P.L, KDA);
+template <typename IO, bool KDA, int K>
+static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n_layers,
+                                 const CursorArgs &C, const int32_t *slot_idx, int B,
+                                 cudaStream_t stream) {
+    const size_t smem = fold_smem_bytes(K, P.L, KDA);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int grid = 2 * sms;
-#define GDN_FOLD_LAUNCH(KCV)                                                                   \
-    do {                                                                                       \
-        auto kern = fold_kernel<IO, KDA, KCV>;                                                 \
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-        if (e != cudaSuccess) return e;                                                        \
-        kern<<<grid, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B);           \
-    } while (0)
-    if (P.K <= 32) GDN_FOLD_LAUNCH(2);
-    else if (P.K <= 64) GDN_FOLD_LAUNCH(4);
-    else if (P.K <= 128) GDN_FOLD_LAUNCH(8);
-    else GDN_FOLD_LAUNCH(16);
-#undef GDN_FOLD_LAUNCH
+    auto kern = fold_kernel<IO, KDA, K>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<2 * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B);
     return cudaGetLastError();
 }
 
-bool fold_supported(int K, int L) { return K <= 256 && L <= kFoldMaxL; }
+template <typename IO, bool KDA>
+static cudaError_t launch_fold_typed(const LayerArgs &P, const FoldLayers &FL, int n_layers,
+                                     const CursorArgs &C, const int32_t *slot_idx, int B,
+                                     cudaStream_t stream) {
+    switch (P.K) {
+        case 32: return launch_fold_k<IO, KDA, 32>(P, FL, n_layers, C, slot_idx, B, stream);
+        case 64: return launch_fold_k<IO, KDA, 64>(P, FL, n_layers, C, slot_idx, B, stream);
+        case 128: return launch_fold_k<IO, KDA, 128>(P, FL, n_layers, C, slot_idx, B, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+bool fold_supported(int K, int L) { return (K == 32 || K == 64 || K == 128) && L <= kFoldMaxL; }
 
 cudaError_t launch_fold(const LayerArgs &P, const FoldLayers &FL, int n_layers, bool kda,
                         bool bf16, const CursorArgs &C, const int32_t *slot_idx, int B,

@@ -52,7 +52,7 @@ constexpr int kXRows = 80;         // Gram N (keys + queries, padded to 16)
 constexpr int kXAtom = kXRows * 128;   // bytes of one 32-float K slice of X
 constexpr int kS0Atom = kBV * 128;     // bytes of one 32-float K slice of S0
 constexpr int kQAtom = 16 * 128;       // bytes of one K slice of q_eff (N = 16)
-constexpr int kALd = kLMax;            // row stride (floats) of A (zero above the diagonal)
+constexpr int kALd = kLMax + 4;        // row stride (floats) of A: 16-byte rows, conflict-free
 
 // Shared-memory map (bytes from a 1024-aligned base).  R0 holds first the key
 // phase (X, A, F, gates, decay products), then the checkpoint tile.  R1 is
@@ -61,8 +61,8 @@ constexpr int kALd = kLMax;            // row stride (floats) of A (zero above t
 // hold c = M beta for the output.
 constexpr int kOffX = 0;
 constexpr int kOffA = kOffX + 4 * kXAtom;                     // 40960
-constexpr int kOffF = kOffA + kLMax * kALd * 4;               // 57344: F, then c eG
-constexpr int kOffAlpha = kOffF + kLMax * kTMax * 4;          // 59392
+constexpr int kOffF = kOffA + kLMax * kALd * 4;               // 58368: F, then c eG
+constexpr int kOffAlpha = kOffF + kLMax * kTMax * 4;          // 60416
 constexpr int kOffBeta = kOffAlpha + kLMax * 4;
 constexpr int kOffEG = kOffBeta + kLMax * 4;
 constexpr int kOffSuf = kOffEG + kLMax * 4;                   // suffix products, L+1 floats
@@ -182,25 +182,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         __nv_bfloat16 *rawv_w = reinterpret_cast<__nv_bfloat16 *>(P.rawv);
         const bool k_writer = (hv % P.G == 0) && vb == 0;
 
-        // ---- 1. one round of global reads: keys (rows 0..n-1), queries (rows
-        //         64..), gate inputs of token tid, window values of row tid
-        constexpr int kRowsPerWarp = (kLMax + kTMax) / 4;  // 18
-        uint2 raw[kRowsPerWarp];
-#pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-            const int t = warp + 4 * i;  // token index: keys 0..n-1, then queries
-            raw[i] = make_uint2(0u, 0u);
-            if (t < n + T) {
-                const __nv_bfloat16 *src;
-                if (t < W)
-                    src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
-                else if (t < n)
-                    src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
-                else
-                    src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
-                raw[i] = reinterpret_cast<const uint2 *>(src)[lane];
-            }
-        }
+        // ---- 1. global reads: two threads per token row (keys 0..n-1, then the
+        //         T queries), 128 bytes each as 8 x 16 B; the gate inputs of
+        //         token tid and the window values of state row tid
         float g_in = 0.f, b_in = 0.f, alog = 0.f, dtb = 0.f;
         const int pj = ring_pos(base, tid, L);
         if (tid < W) {
@@ -218,24 +202,60 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         for (int s = 0; s < TM; ++s)
             vwin_raw[s] = (s < T && vrow < V) ? v[(((size_t)bb * T + s) * HV + hv) * V + vrow]
                                                : __float2bfloat16_rn(0.0f);
-
-        // normalise into X (SW128 K-major), ring side channel for the window keys
+        const int half = tid & 1;
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1 && n + T <= 64) break;  // a second pass only when W > L - 2T
+            const int t = (tid >> 1) + 64 * pass;
+            const bool has_row = t < n + T;
+            const __nv_bfloat16 *src = q;
+            if (t < W)
+                src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
+            else if (t < n)
+                src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
+            else if (has_row)
+                src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
+            uint4 raw[8];
 #pragma unroll
-        for (int i = 0; i < kRowsPerWarp; ++i) {
-            const int t = warp + 4 * i;
-            if (t < n + T) {
-                const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i].x);
-                const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162 *>(&raw[i].y);
-                const float2 f0 = __bfloat1622float2(lo), f1 = __bfloat1622float2(hi);
-                float ss = f0.x * f0.x + f0.y * f0.y + f1.x * f1.x + f1.y * f1.y;
-                ss = warp_sum(ss);
-                const float r = 1.0f / sqrtf(ss + P.l2_eps);
+            for (int c = 0; c < 8; ++c)
+                raw[c] = has_row ? reinterpret_cast<const uint4 *>(src)[8 * half + c]
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                    ss[e] = fmaf(f.x, f.x, ss[e]);
+                    ss[e] = fmaf(f.y, f.y, ss[e]);
+                }
+            }
+            float sq = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 1);   // the row's other half
+            if (has_row) {
+                const float r = 1.0f / sqrtf(sq + P.l2_eps);
                 const int row = t < n ? t : kQRow + (t - n);
-                *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, 4 * lane)) =
-                    make_float4(f0.x * r, f0.y * r, f1.x * r, f1.y * r);
-                if (t >= W && t < n && k_writer)
-                    reinterpret_cast<uint2 *>(rawk_w + (sh_h * L + ring_pos(base, t, L)) * kK)[lane] =
-                        raw[i];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // chunk c of this half: k = 64 half + 8c .. + 7
+                    const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                        f[2 * e] = x.x * r;
+                        f[2 * e + 1] = x.y * r;
+                    }
+                    const int k0 = 64 * half + 8 * c;
+                    *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, k0)) =
+                        make_float4(f[0], f[1], f[2], f[3]);
+                    *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, k0 + 4)) =
+                        make_float4(f[4], f[5], f[6], f[7]);
+                }
+                if (t >= W && t < n && k_writer) {  // side channel: raw key, bitwise
+                    uint4 *dst = reinterpret_cast<uint4 *>(rawk_w + (sh_h * L + ring_pos(base, t, L)) * kK);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) dst[8 * half + c] = raw[c];
+                }
             }
         }
         if (tid < n) {
@@ -306,29 +326,36 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         {
             const int i = tid;
             const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + kGramCol;
+            // tcgen05.ld is warp-collective: every load below runs on all lanes
             float gq[16];
             ptx::tmem_ld16(tbase + kQRow, gq);   // columns 64..79: the query columns
-            float gk[64];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float r[16];
-                ptx::tmem_ld16(tbase + 16 * c, r);
-#pragma unroll
-                for (int x = 0; x < 16; ++x) gk[16 * c + x] = r[x];
-            }
             ptx::tmem_ld_wait();
-            if (i < n) {
-                const float bi = betaS[i];
-                float c = 1.0f;
+            const bool row_live = i < n;
+            const float bi = row_live ? betaS[i] : 0.0f;
+            float c = 1.0f;
+#pragma unroll 1
+            for (int cc = kLMax / 16 - 1; cc >= 0; --cc) {  // key columns, high chunk first
+                float gk[16];
+                ptx::tmem_ld16(tbase + 16 * cc, gk);
+                ptx::tmem_ld_wait();
+                if (row_live) {
+                    float val[16];
 #pragma unroll
-                for (int r = kLMax - 1; r >= 0; --r) {
-                    float val = 0.0f;
-                    if (r < i) {
-                        c *= alpha[r + 1];               // Gamma(i, r)
-                        val = bi * c * gk[r];
+                    for (int x = 15; x >= 0; --x) {
+                        const int r = 16 * cc + x;
+                        val[x] = 0.0f;
+                        if (r < i) {
+                            c *= alpha[r + 1];               // Gamma(i, r)
+                            val[x] = bi * c * gk[x];
+                        }
                     }
-                    A[i * kALd + r] = val;
+#pragma unroll
+                    for (int x = 0; x < 16; x += 4)
+                        *reinterpret_cast<float4 *>(A + i * kALd + 16 * cc + x) =
+                            make_float4(val[x], val[x + 1], val[x + 2], val[x + 3]);
                 }
+            }
+            if (row_live) {
                 // Gamma(W+s, i): products of the suffix and window decays
                 const float si = i < W ? suf[i + 1] : 1.0f;
                 float cw = 1.0f;
@@ -355,20 +382,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         if (!waited && tid == 0) misc[5] = 1;
         __syncthreads();
 
-        // the v history of this thread's row (L2-resident), held for the output
-        // (two bf16 per register)
-        __nv_bfloat162 rv[kLMax / 2];
-#pragma unroll
-        for (int jp = 0; jp < kLMax / 2; ++jp) {
-            const int j0 = 2 * jp, j1 = 2 * jp + 1;
-            const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
-            const __nv_bfloat16 x0 =
-                (j0 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j0, L)) * V + vrow] : z;
-            const __nv_bfloat16 x1 =
-                (j1 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j1, L)) * V + vrow] : z;
-            rv[jp] = __halves2bfloat162(x0, x1);
-        }
-
         // ---- 4. M (I + A) = F^T, all T rows in warp 0; lane l ends with M[s][l], M[s][l+32]
         if (warp == 0) {
             float f0[TM], f1[TM];
@@ -377,7 +390,38 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 f0[s] = lane < n ? F[lane * TM + s] : 0.0f;
                 f1[s] = lane + 32 < n ? F[(lane + 32) * TM + s] : 0.0f;
             }
-            for (int j = n - 1; j >= 0; --j) {
+            // four tokens j-3..j per step: the 4 x 4 diagonal block is solved
+            // redundantly on every lane, then all lanes apply the four updates
+            // (which also leave f[j-3..j] equal to their final values)
+            int j = n - 1;
+            for (; j >= 3; j -= 4) {
+                float a[4][2], d[6];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    a[q][0] = A[(j - q) * kALd + lane];
+                    a[q][1] = A[(j - q) * kALd + 32 + lane];
+                }
+                d[0] = A[j * kALd + j - 1];        // A[j][j-1]
+                d[1] = A[j * kALd + j - 2];        // A[j][j-2]
+                d[2] = A[j * kALd + j - 3];        // A[j][j-3]
+                d[3] = A[(j - 1) * kALd + j - 2];  // A[j-1][j-2]
+                d[4] = A[(j - 1) * kALd + j - 3];  // A[j-1][j-3]
+                d[5] = A[(j - 2) * kALd + j - 3];  // A[j-2][j-3]
+#pragma unroll
+                for (int s = 0; s < TM; ++s) {
+                    float fj[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        fj[q] = __shfl_sync(0xffffffffu, (j - q) < 32 ? f0[s] : f1[s], (j - q) & 31);
+                    const float m0 = fj[0];
+                    const float m1 = fmaf(-d[0], m0, fj[1]);
+                    const float m2 = fmaf(-d[3], m1, fmaf(-d[1], m0, fj[2]));
+                    const float m3 = fmaf(-d[5], m2, fmaf(-d[4], m1, fmaf(-d[2], m0, fj[3])));
+                    f0[s] = fmaf(-a[3][0], m3, fmaf(-a[2][0], m2, fmaf(-a[1][0], m1, fmaf(-a[0][0], m0, f0[s]))));
+                    f1[s] = fmaf(-a[3][1], m3, fmaf(-a[2][1], m2, fmaf(-a[1][1], m1, fmaf(-a[0][1], m0, f1[s]))));
+                }
+            }
+            for (; j >= 0; --j) {
                 const float a0 = A[j * kALd + lane], a1 = A[j * kALd + 32 + lane];
 #pragma unroll
                 for (int s = 0; s < TM; ++s) {
@@ -448,6 +492,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             for (int kb = 0; kb < 4; ++kb)
                 ptx::tma_load_2d(sm_s + kOffS0 + kb * kS0Atom, &tmap_s0, bar_s0, kb * 32, y);
         }
+        // the v history of this thread's row (prefetched to L2 at the start);
+        // these loads overlap the checkpoint tile's TMA
+        // (two bf16 per register)
+        __nv_bfloat162 rv[kLMax / 2];
+#pragma unroll
+        for (int jp = 0; jp < kLMax / 2; ++jp) {
+            const int j0 = 2 * jp, j1 = 2 * jp + 1;
+            const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
+            const __nv_bfloat16 x0 =
+                (j0 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j0, L)) * V + vrow] : z;
+            const __nv_bfloat16 x1 =
+                (j1 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j1, L)) * V + vrow] : z;
+            rv[jp] = __halves2bfloat162(x0, x1);
+        }
+
         // output part that does not need the checkpoint: sum_j c[j][s] v_j
         float vt[TM];
 #pragma unroll

@@ -93,7 +93,7 @@ extern "C" {
 typedef struct {
     int32_t H;          /* q/k heads                                               */
     int32_t HV;         /* v heads; H divides HV; v-head hv uses q/k head hv / (HV/H) */
-    int32_t K;          /* key dim (multiple of 8, <= 256)                         */
+    int32_t K;          /* key dim: 32, 64 or 128                                  */
     int32_t V;          /* value dim (multiple of 8)                               */
     int32_t T;          /* draft window (tokens per row per verify), 1..16         */
     int32_t L;          /* ring length: a power of two, >= 2T ([pr28695] config check) */
@@ -139,8 +139,9 @@ typedef struct {
  *   out       io_dtype [B, T, HV, V]  (written)
  *
  * Device status: SLOT_OOR, CURSOR_CORRUPT, RING_OVERFLOW (the row is skipped
- * and its outputs are zero).  Supported shapes: K <= 256; L <= 128 (GATE_SCALAR)
- * or L <= 64 (GATE_PER_KEY); T <= 16; otherwise GDN_SPEC_EUNSUPPORTED.
+ * and its outputs are zero).  Supported shapes: K in {32, 64, 128}; L <= 128
+ * (GATE_SCALAR) or L <= 64 (GATE_PER_KEY); T <= 16; otherwise
+ * GDN_SPEC_EUNSUPPORTED.
  */
 int gdn_spec_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
                     const int32_t *slot_idx, int32_t B,
