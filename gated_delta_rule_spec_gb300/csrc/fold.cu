@@ -8,14 +8,14 @@
 //     S <- exp(g_t) S   (KDA: S diag(exp(g_t)))
 //     d  = beta_t (v_t - S k^_t),   S <- S + d k^_t^T
 // Rows of S are independent under the recurrence (row i only sees v_t[i]),
-// so one thread owns one state row: its K values live in registers, the dot
-// product needs no shuffles, and the records are replayed one after another.
+// so four threads own one state row (K/4 values each, in registers; the row's
+// dot product takes two shuffles) and replay the records one after another.
 // The elementwise work uses Blackwell's packed fp32x2 instructions.
 //
 // Only the rows whose is_flush is set do any work, and in steady state that
 // is a small share of the batch per step.  So the grid is persistent: every
 // CTA scans the batch's flags, builds the same compact list of rows to fold,
-// and takes work items (row, layer, v-head, block of 128 state rows)
+// and takes work items (row, layer, v-head, block of 32 state rows)
 // round-robin from it.  For an item every global read (keys, gates, values,
 // the state rows) is issued in one round.  Folding runs after sampling,
 // outside the forward, so the layers are independent here and one launch
@@ -26,21 +26,24 @@
 namespace gdnspec {
 
 constexpr int kFoldThreads = 128;
+constexpr int kFoldTPR = 4;                          // threads per state row
+constexpr int kFoldRows = kFoldThreads / kFoldTPR;   // state rows per work item
 constexpr int kFoldMaxL = 128;   // ring length limit of this kernel
 constexpr int kFoldScan = kFoldThreads;
 
 // Shared memory of one item: raw keys [L][K] fp32, alpha [L] (KDA [L][K]),
-// beta [L], 1/|k| [L], values [L][128 rows] fp32, and the compacted row list.
+// beta [L], 1/|k| [L], values [L][32 rows] fp32, and the compacted row list.
 size_t fold_smem_bytes(int K, int L, bool kda) {
-    return sizeof(float) * ((size_t)L * K + (size_t)L * (kda ? K : 1) + 2 * L + (size_t)L * kFoldThreads) +
+    return sizeof(float) * ((size_t)L * K + (size_t)L * (kda ? K : 1) + 2 * L + (size_t)L * kFoldRows) +
            sizeof(int) * 2 * kFoldScan;
 }
 
 template <typename IO, bool KDA, int K>
-__global__ void __launch_bounds__(kFoldThreads, 2)
+__global__ void __launch_bounds__(kFoldThreads, 4)
 fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int32_t *__restrict__ slot_idx, int B) {
-    static_assert(K % 8 == 0 && K <= 128, "one state row per thread");
+    static_assert(K % 32 == 0 && K <= 128, "K/4 state values per thread, in float4 chunks");
+    constexpr int KC = K / 16;   // float4 chunks per thread: chunk c4 = part + 4 m
     extern __shared__ __align__(16) float sm[];
     __shared__ int s_count, s_warp_off[kFoldThreads / 32];
     const int V = P.V, L = P.L, HV = P.HV, H = P.H;
@@ -49,10 +52,10 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     float *alpha = Xs + (size_t)L * K;               // [L] or [L][K]
     float *betaS = alpha + (size_t)L * (KDA ? K : 1);
     float *rsS = betaS + L;                          // [L] 1 / |k_t|
-    float *vv = rsS + L;                             // [L][kFoldThreads]
-    int *rows = reinterpret_cast<int *>(vv + (size_t)L * kFoldThreads);
+    float *vv = rsS + L;                             // [L][kFoldRows]
+    int *rows = reinterpret_cast<int *>(vv + (size_t)L * kFoldRows);
     int *meta = rows + kFoldScan;
-    const int vblocks = (V + kFoldThreads - 1) / kFoldThreads;
+    const int vblocks = (V + kFoldRows - 1) / kFoldRows;
     const int per_row = n_layers * HV * vblocks;
     long long item_base = 0;  // items enumerated in earlier scan passes
 
@@ -101,7 +104,8 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int h = hv / P.G;
             const int slot = slot_idx[rows[e]];
             const int W = meta[e] >> 16, base = meta[e] & 0xFFFF;
-            const int vr = vbk * kFoldThreads + tid;   // this thread's state row
+            const int r = tid / kFoldTPR, part = tid % kFoldTPR;
+            const int vr = vbk * kFoldRows + r;   // this thread's state row
             const bool valid = vr < V;
             const size_t sh_hv = (size_t)slot * HV + hv, sh_h = (size_t)slot * H + h;
             const IO *rawk = reinterpret_cast<const IO *>(FL.rawk[li]);
@@ -110,15 +114,15 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const float *ring_beta = FL.ring_beta[li];
             float *ckpt = FL.checkpoint[li];
 
-            // ---- one round of reads: the state row, keys (two threads per
-            //      record), gates (thread per record), values (thread per row)
-            float2 S2[K / 2];
+            // ---- one round of reads: the state row slice, keys (two threads per
+            //      record), gates (thread per record), values
+            float2 S2[2 * KC];
             const float4 *srow = reinterpret_cast<const float4 *>(ckpt + (sh_hv * V + (valid ? vr : 0)) * K);
 #pragma unroll
-            for (int c = 0; c < K / 4; ++c) {
-                const float4 t4 = valid ? srow[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-                S2[2 * c] = make_float2(t4.x, t4.y);
-                S2[2 * c + 1] = make_float2(t4.z, t4.w);
+            for (int m = 0; m < KC; ++m) {
+                const float4 t4 = valid ? srow[part + 4 * m] : make_float4(0.f, 0.f, 0.f, 0.f);
+                S2[2 * m] = make_float2(t4.x, t4.y);
+                S2[2 * m + 1] = make_float2(t4.z, t4.w);
             }
             // keys stay raw in shared memory; rs[t] = 1 / |k_t| (with eps) is
             // applied in the replay, so no key slice is held in registers
@@ -169,66 +173,67 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             }
             for (int j = tid; j < W; j += kFoldThreads)
                 betaS[j] = ring_beta[sh_hv * L + ring_pos(base, j, L)];
-            for (int j0 = 0; j0 < W; j0 += 16) {
-                float xv[16];
+            {   // values: thread (row r, part) loads records part, part + 4, ...
+                float xv[kFoldMaxL / kFoldTPR];
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    xv[u] = (j0 + u < W && valid)
-                                ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j0 + u, L)) * V + vr])
+                for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
+                    const int j = part + kFoldTPR * u;
+                    xv[u] = (j < W && valid)
+                                ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vr])
                                 : 0.0f;
+                }
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (j0 + u < W) vv[(j0 + u) * kFoldThreads + tid] = xv[u];
+                for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
+                    const int j = part + kFoldTPR * u;
+                    if (j < W) vv[j * kFoldRows + r] = xv[u];
+                }
             }
             __syncthreads();
 
             // ---- replay (decay, then the delta against the decayed state)
             for (int t = 0; t < W; ++t) {
                 const float4 *xk = reinterpret_cast<const float4 *>(Xs + t * K);
-                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                                 make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 if (KDA) {
                     const float4 *al = reinterpret_cast<const float4 *>(alpha + (size_t)t * K);
 #pragma unroll
-                    for (int c = 0; c < K / 4; ++c) {
-                        const float4 a4 = al[c], x4 = xk[c];
-                        S2[2 * c] = __fmul2_rn(S2[2 * c], make_float2(a4.x, a4.y));
-                        S2[2 * c + 1] = __fmul2_rn(S2[2 * c + 1], make_float2(a4.z, a4.w));
-                        acc[c & 3] = __ffma2_rn(S2[2 * c], make_float2(x4.x, x4.y), acc[c & 3]);
-                        acc[c & 3] = __ffma2_rn(S2[2 * c + 1], make_float2(x4.z, x4.w), acc[c & 3]);
+                    for (int m = 0; m < KC; ++m) {
+                        const float4 a4 = al[part + 4 * m], x4 = xk[part + 4 * m];
+                        S2[2 * m] = __fmul2_rn(S2[2 * m], make_float2(a4.x, a4.y));
+                        S2[2 * m + 1] = __fmul2_rn(S2[2 * m + 1], make_float2(a4.z, a4.w));
+                        acc[0] = __ffma2_rn(S2[2 * m], make_float2(x4.x, x4.y), acc[0]);
+                        acc[1] = __ffma2_rn(S2[2 * m + 1], make_float2(x4.z, x4.w), acc[1]);
                     }
                 } else {
                     const float a = alpha[t];
                     const float2 a2 = make_float2(a, a);
 #pragma unroll
-                    for (int c = 0; c < K / 4; ++c) {
-                        const float4 x4 = xk[c];
-                        S2[2 * c] = __fmul2_rn(S2[2 * c], a2);
-                        S2[2 * c + 1] = __fmul2_rn(S2[2 * c + 1], a2);
-                        acc[c & 3] = __ffma2_rn(S2[2 * c], make_float2(x4.x, x4.y), acc[c & 3]);
-                        acc[c & 3] = __ffma2_rn(S2[2 * c + 1], make_float2(x4.z, x4.w), acc[c & 3]);
+                    for (int m = 0; m < KC; ++m) {
+                        const float4 x4 = xk[part + 4 * m];
+                        S2[2 * m] = __fmul2_rn(S2[2 * m], a2);
+                        S2[2 * m + 1] = __fmul2_rn(S2[2 * m + 1], a2);
+                        acc[0] = __ffma2_rn(S2[2 * m], make_float2(x4.x, x4.y), acc[0]);
+                        acc[1] = __ffma2_rn(S2[2 * m + 1], make_float2(x4.z, x4.w), acc[1]);
                     }
                 }
+                float u = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+                u += __shfl_xor_sync(0xffffffffu, u, 1);
+                u += __shfl_xor_sync(0xffffffffu, u, 2);
                 const float rs = rsS[t];
-                const float u = rs * (((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
-                                      ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y)));
-                const float d = betaS[t] * (vv[t * kFoldThreads + tid] - u) * rs;
+                const float d = betaS[t] * (vv[t * kFoldRows + r] - rs * u) * rs;
                 const float2 d2 = make_float2(d, d);
-                // re-read the key from shared memory below rather than keeping
-                // all K values of it in registers across the dot product
-                asm volatile("" ::: "memory");
 #pragma unroll
-                for (int c = 0; c < K / 4; ++c) {
-                    const float4 x4 = xk[c];
-                    S2[2 * c] = __ffma2_rn(d2, make_float2(x4.x, x4.y), S2[2 * c]);
-                    S2[2 * c + 1] = __ffma2_rn(d2, make_float2(x4.z, x4.w), S2[2 * c + 1]);
+                for (int m = 0; m < KC; ++m) {
+                    const float4 x4 = xk[part + 4 * m];
+                    S2[2 * m] = __ffma2_rn(d2, make_float2(x4.x, x4.y), S2[2 * m]);
+                    S2[2 * m + 1] = __ffma2_rn(d2, make_float2(x4.z, x4.w), S2[2 * m + 1]);
                 }
             }
             if (valid) {
                 float4 *dst = reinterpret_cast<float4 *>(ckpt + (sh_hv * V + vr) * K);
 #pragma unroll
-                for (int c = 0; c < K / 4; ++c)
-                    dst[c] = make_float4(S2[2 * c].x, S2[2 * c].y, S2[2 * c + 1].x, S2[2 * c + 1].y);
+                for (int m = 0; m < KC; ++m)
+                    dst[part + 4 * m] = make_float4(S2[2 * m].x, S2[2 * m].y, S2[2 * m + 1].x, S2[2 * m + 1].y);
             }
             __syncthreads();  // the item's buffers are reused by the next item
         }
@@ -249,7 +254,9 @@ static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n
     auto kern = fold_kernel<IO, KDA, K>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<2 * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B);
+    // enough CTAs for every item of a typical step to run at once; the ones
+    // without an item leave after the flag scan
+    kern<<<4 * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B);
     return cudaGetLastError();
 }
 

@@ -494,19 +494,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         }
         // the v history of this thread's row (prefetched to L2 at the start);
         // these loads overlap the checkpoint tile's TMA
-        // (two bf16 per register)
-        __nv_bfloat162 rv[kLMax / 2];
+        float rv[kLMax];
 #pragma unroll
-        for (int jp = 0; jp < kLMax / 2; ++jp) {
-            const int j0 = 2 * jp, j1 = 2 * jp + 1;
-            const __nv_bfloat16 z = __float2bfloat16_rn(0.0f);
-            const __nv_bfloat16 x0 =
-                (j0 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j0, L)) * V + vrow] : z;
-            const __nv_bfloat16 x1 =
-                (j1 < W && vrow < V) ? rawv[(sh_hv * L + ring_pos(base, j1, L)) * V + vrow] : z;
-            rv[jp] = __halves2bfloat162(x0, x1);
-        }
-
+        for (int j = 0; j < kLMax; ++j)
+            rv[j] = (j < W && vrow < V)
+                        ? __bfloat162float(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vrow])
+                        : 0.0f;
         // output part that does not need the checkpoint: sum_j c[j][s] v_j
         float vt[TM];
 #pragma unroll
@@ -517,9 +510,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             const bool hist = j < kLMax;
             const int jj = hist ? j : W + (j - kLMax);
             if (hist ? j < W : (j - kLMax) < T) {
-                const float x = hist ? ((j & 1) ? __high2float(rv[hist ? j >> 1 : 0])
-                                                : __low2float(rv[hist ? j >> 1 : 0]))
-                                     : __bfloat162float(vwin_raw[hist ? 0 : j - kLMax]);
+                const float x = hist ? rv[hist ? j : 0] : __bfloat162float(vwin_raw[hist ? 0 : j - kLMax]);
 #pragma unroll
                 for (int s = 0; s < TM; s += 4) {
                     const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(jj) + 4 * s);
