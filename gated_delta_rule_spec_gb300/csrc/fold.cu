@@ -125,19 +125,51 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                 S2[2 * m + 1] = make_float2(t4.z, t4.w);
             }
             // keys stay raw in shared memory; rs[t] = 1 / |k_t| (with eps) is
-            // applied in the replay, so no key slice is held in registers
-            for (int pass = 0; pass * (kFoldThreads / 2) < W; ++pass) {
-                const int j = pass * (kFoldThreads / 2) + (tid >> 1), half = tid & 1;
-                constexpr int KH = K / 2;   // elements per thread
-                constexpr int kPer = 16 / (int)sizeof(IO);
-                float ss = 0.0f;
+            // applied in the replay.  All loads of the item are issued before
+            // any of them is used: keys of records tid/2 (+64 per pass), the
+            // gates of record tid, the values of this thread's records.
+            constexpr int KH = K / 2;                    // key elements per thread
+            constexpr int kPer = 16 / (int)sizeof(IO);
+            constexpr int kChunks = KH / kPer;
+            const int half = tid & 1;
+            uint4 kraw[kChunks];
+            {
+                const int j = tid >> 1;
                 if (j < W) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(
                         rawk + (sh_h * L + ring_pos(base, j, L)) * K + half * KH);
 #pragma unroll
-                    for (int c = 0; c < KH / kPer; ++c) {
+                    for (int c = 0; c < kChunks; ++c) kraw[c] = src[c];
+                }
+            }
+            float g_in = 0.f, b_in = 0.f;
+            if (tid < W) {
+                const int p = ring_pos(base, tid, L);
+                if (!KDA) g_in = ring_g[sh_hv * L + p];
+                b_in = ring_beta[sh_hv * L + p];
+            }
+            float xv[kFoldMaxL / kFoldTPR];
+#pragma unroll
+            for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
+                const int j = part + kFoldTPR * u;
+                xv[u] = (j < W && valid) ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vr])
+                                         : 0.0f;
+            }
+            // keys -> shared memory (first 64 records from the registers above)
+            for (int pass = 0; pass * (kFoldThreads / 2) < W; ++pass) {
+                const int j = pass * (kFoldThreads / 2) + (tid >> 1);
+                if (pass > 0 && j < W) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        rawk + (sh_h * L + ring_pos(base, j, L)) * K + half * KH);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) kraw[c] = src[c];
+                }
+                float ss = 0.0f;
+                if (j < W) {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
                         float x[kPer];
-                        const uint4 u4 = src[c];
+                        const uint4 u4 = kraw[c];
                         if constexpr (sizeof(IO) == 2) {
                             const uint32_t w[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
@@ -167,26 +199,18 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                     const int j = idx / K, kk = idx - j * K;
                     alpha[idx] = expf(ring_g[(sh_hv * L + ring_pos(base, j, L)) * K + kk]);
                 }
-            } else {
-                for (int j = tid; j < W; j += kFoldThreads)
-                    alpha[j] = expf(ring_g[sh_hv * L + ring_pos(base, j, L)]);
+            } else if (tid < W) {
+                alpha[tid] = expf(g_in);
             }
-            for (int j = tid; j < W; j += kFoldThreads)
+            if (tid < W) betaS[tid] = b_in;
+            for (int j = kFoldThreads + tid; j < W; j += kFoldThreads) {  // records >= 128 (none: L <= 128)
+                if (!KDA) alpha[j] = expf(ring_g[sh_hv * L + ring_pos(base, j, L)]);
                 betaS[j] = ring_beta[sh_hv * L + ring_pos(base, j, L)];
-            {   // values: thread (row r, part) loads records part, part + 4, ...
-                float xv[kFoldMaxL / kFoldTPR];
+            }
 #pragma unroll
-                for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
-                    const int j = part + kFoldTPR * u;
-                    xv[u] = (j < W && valid)
-                                ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vr])
-                                : 0.0f;
-                }
-#pragma unroll
-                for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
-                    const int j = part + kFoldTPR * u;
-                    if (j < W) vv[j * kFoldRows + r] = xv[u];
-                }
+            for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
+                const int j = part + kFoldTPR * u;
+                if (j < W) vv[j * kFoldRows + r] = xv[u];
             }
             __syncthreads();
 
