@@ -128,7 +128,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
     float *wprod = reinterpret_cast<float *>(sm + kOffWP);
     int *misc = reinterpret_cast<int *>(sm + kOffMisc);  // slot, base, W, ok, tmem, err
     const uint32_t bar_gram = sm_s + kOffBar, bar_s0 = sm_s + kOffBar + 8,
-                   bar_p = sm_s + kOffBar + 16;
+                   bar_p = sm_s + kOffBar + 16, bar_vh = sm_s + kOffBar + 24;
+    // v history of this CTA's rows, staged over the dead A matrix: [W][kBV] bf16
+    const __nv_bfloat16 *vh = reinterpret_cast<const __nv_bfloat16 *>(sm + kOffA);
 
     const int hv = blockIdx.x, bb = blockIdx.y, vb = blockIdx.z;
     const int T = P.T, L = P.L, HV = P.HV, H = P.H, V = P.V;
@@ -149,6 +151,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         ptx::mbar_init(bar_gram, 1);
         ptx::mbar_init(bar_s0, 1);
         ptx::mbar_init(bar_p, 1);
+        ptx::mbar_init(bar_vh, 1);
         ptx::mbar_init_fence();
         ptx::prefetch_tmap(&tmap_s0);
         if (ok) {  // checkpoint tile and v history into L2 now; used at the end
@@ -452,6 +455,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         }
         __syncthreads();
 
+        // ---- 5a. the v history of this CTA's rows into the (now dead) A
+        //          matrix: one 1-D bulk copy per record, spread over warp 0
+        if (warp == 0) {
+            ptx::fence_proxy_async_smem();   // the A matrix was last read by generic loads
+            if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)W * kBV * 2);
+            __syncwarp();
+            for (int j = lane; j < W; j += 32)
+                ptx::bulk_copy_g2s(sm_s + kOffA + j * kBV * 2,
+                                   rawv + (sh_hv * L + ring_pos(base, j, L)) * V + v0, kBV * 2,
+                                   bar_vh);
+        }
         // ---- 5. q_eff (thread = key channel): eG_{W+s} q^_s - sum_j c[j][s] eG_j k^_j
         {
             const int kk = tid;
@@ -480,6 +494,40 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             for (int s = 0; s < TM; ++s)
                 if (s < T) *reinterpret_cast<float *>(sm + kOffQ + sw128(kQAtom, s, kk)) = acc[s];
         }
+        // output part that does not need the checkpoint: sum_j c[j][s] v_j,
+        // from the staged v history and the window values
+        float vt[TM];
+#pragma unroll
+        for (int s = 0; s < TM; ++s) vt[s] = 0.0f;
+        bool vh_ok = W == 0 || ptx::mbar_wait(bar_vh, 0);
+        if (vrow < V) {
+            for (int j = 0; j < W; ++j) {
+                const float x = __bfloat162float(vh[j * kBV + tid]);
+#pragma unroll
+                for (int s = 0; s < TM; s += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(j) + 4 * s);
+                    vt[s] = fmaf(c4.x, x, vt[s]);
+                    vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
+                    vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
+                    vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
+                }
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < TM; ++s2) {
+                if (s2 < T) {
+                    const float x = __bfloat162float(vwin_raw[s2]);
+#pragma unroll
+                    for (int s = 0; s < TM; s += 4) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(W + s2) + 4 * s);
+                        vt[s] = fmaf(c4.x, x, vt[s]);
+                        vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
+                        vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
+                        vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
+                    }
+                }
+            }
+        }
+        if (!vh_ok && tid == 0) misc[5] = 1;
         ptx::fence_proxy_async_smem();
         __syncthreads();
 
@@ -491,35 +539,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb)
                 ptx::tma_load_2d(sm_s + kOffS0 + kb * kS0Atom, &tmap_s0, bar_s0, kb * 32, y);
-        }
-        // the v history of this thread's row (prefetched to L2 at the start);
-        // these loads overlap the checkpoint tile's TMA
-        float rv[kLMax];
-#pragma unroll
-        for (int j = 0; j < kLMax; ++j)
-            rv[j] = (j < W && vrow < V)
-                        ? __bfloat162float(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vrow])
-                        : 0.0f;
-        // output part that does not need the checkpoint: sum_j c[j][s] v_j
-        float vt[TM];
-#pragma unroll
-        for (int s = 0; s < TM; ++s) vt[s] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kLMax + TM; ++j) {
-            // history records j < W from registers, then the window values
-            const bool hist = j < kLMax;
-            const int jj = hist ? j : W + (j - kLMax);
-            if (hist ? j < W : (j - kLMax) < T) {
-                const float x = hist ? rv[hist ? j : 0] : __bfloat162float(vwin_raw[hist ? 0 : j - kLMax]);
-#pragma unroll
-                for (int s = 0; s < TM; s += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(jj) + 4 * s);
-                    vt[s] = fmaf(c4.x, x, vt[s]);
-                    vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
-                    vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
-                    vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
-                }
-            }
         }
         waited = ptx::mbar_wait(bar_s0, 0);
         if (tid == 0) {
