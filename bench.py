@@ -74,7 +74,7 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_spec_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("verify") or name == "common.cuh":
+        if name.startswith("verify") or name in ("common.cuh", "ptx_sm100.cuh"):
             h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
