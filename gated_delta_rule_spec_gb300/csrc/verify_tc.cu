@@ -106,14 +106,101 @@ __device__ __forceinline__ float warp_prefix_prod(float x, int lane) {
     return x;
 }
 
+// One unit = (batch row, v-head, block of 128 state rows).  Fetching a unit
+// means reading its slot and cursors (one thread) and prefetching its
+// checkpoint tile and v history into L2.
+struct UnitInfo {
+    int slot, base, W, ok;
+};
+
+__device__ __forceinline__ void fetch_unit(const LayerArgs &P, const CursorArgs &C,
+                                           const int32_t *slot_idx, int u, int nunits, int VB,
+                                           int *dst) {
+    if (u >= nunits) {
+        dst[0] = -1; dst[1] = 0; dst[2] = 0; dst[3] = 0;
+        return;
+    }
+    const int hv = u % P.HV, rest = u / P.HV, vb = rest % VB, bb = rest / VB;
+    int slot = slot_idx[bb], base = 0, W = 0;
+    uint32_t st = 0;
+    const bool ok = row_cursor_ok(C, slot, P.T, P.L, &base, &W, &st);
+    if (st && vb == 0 && hv == 0) atomicOr(C.status, st);
+    if (ok) {  // checkpoint tile and v history into L2; used at the end of the unit
+        const size_t sh_hv = (size_t)slot * P.HV + hv;
+        ptx::prefetch_l2(P.checkpoint + (sh_hv * P.V + vb * kBV) * kK, kBV * kK * 4);
+        const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv) + sh_hv * P.L * P.V;
+        if (P.V == kBV) {  // whole records are contiguous: one or two segments
+            const int first = (P.L - base) < W ? (P.L - base) : W;
+            if (first > 0) ptx::prefetch_l2(rv + (size_t)base * P.V, first * P.V * 2);
+            if (W > first) ptx::prefetch_l2(rv, (W - first) * P.V * 2);
+        }
+    }
+    dst[0] = slot; dst[1] = base; dst[2] = W; dst[3] = ok ? 1 : 0;
+}
+
+// The early global reads of a unit, held in registers until its first phase:
+// two threads per token row (keys 0..n-1 then the T queries; 128 bytes each),
+// the gate inputs of token tid and the window values of state row tid.
+template <int TM>
+struct UnitLoads {
+    uint4 raw[8];
+    float g_in, b_in, alog, dtb;
+    __nv_bfloat16 vwin[TM];
+};
+
+template <int TM>
+__device__ __forceinline__ void issue_unit_loads(
+    const LayerArgs &P, const UnitInfo &U, int bb, int hv, int vb, int tid,
+    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+    const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ a,
+    const __nv_bfloat16 *__restrict__ bgate, const float *__restrict__ A_log,
+    const float *__restrict__ dt_bias, UnitLoads<TM> &R) {
+    const int T = P.T, L = P.L, HV = P.HV, H = P.H, V = P.V;
+    const int h = hv / P.G, W = U.W, n = W + T, base = U.base;
+    const size_t sh_hv = (size_t)U.slot * HV + hv, sh_h = (size_t)U.slot * H + h;
+    const __nv_bfloat16 *rawk = reinterpret_cast<const __nv_bfloat16 *>(P.rawk);
+    const int t = tid >> 1, half = tid & 1;
+    const bool has_row = U.ok && t < n + T;
+    const __nv_bfloat16 *src = q;
+    if (t < W)
+        src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
+    else if (t < n)
+        src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
+    else if (has_row)
+        src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        R.raw[c] = has_row ? reinterpret_cast<const uint4 *>(src)[8 * half + c] : make_uint4(0u, 0u, 0u, 0u);
+    R.g_in = R.b_in = R.alog = R.dtb = 0.0f;
+    if (U.ok && tid < W) {
+        const int pj = ring_pos(base, tid, L);
+        R.g_in = P.ring_g[sh_hv * L + pj];
+        R.b_in = P.ring_beta[sh_hv * L + pj];
+    } else if (U.ok && tid < n) {
+        const size_t tok = (size_t)bb * T + (tid - W);
+        R.g_in = __bfloat162float(a[tok * HV + hv]);
+        R.b_in = __bfloat162float(bgate[tok * HV + hv]);
+        R.alog = A_log[hv];
+        R.dtb = dt_bias[hv];
+    }
+    const int vrow = vb * kBV + tid;
+#pragma unroll
+    for (int s = 0; s < TM; ++s)
+        R.vwin[s] = (U.ok && s < T && vrow < V) ? v[(((size_t)bb * T + s) * HV + hv) * V + vrow]
+                                                 : __float2bfloat16_rn(0.0f);
+}
+
+// Persistent: each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
+// While a unit waits for its checkpoint tile and output MMA, the CTA already
+// reads the next unit's cursors and issues that unit's key/gate/value loads.
 template <int TM>
 __global__ void __launch_bounds__(kThreads, 3)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, CursorArgs C,
-                 const int32_t *__restrict__ slot_idx, const __nv_bfloat16 *__restrict__ q,
-                 const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
-                 const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ bgate,
-                 const float *__restrict__ A_log, const float *__restrict__ dt_bias,
-                 __nv_bfloat16 *__restrict__ out) {
+                 const int32_t *__restrict__ slot_idx, int nunits,
+                 const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
+                 const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ a,
+                 const __nv_bfloat16 *__restrict__ bgate, const float *__restrict__ A_log,
+                 const float *__restrict__ dt_bias, __nv_bfloat16 *__restrict__ out) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = ptx::smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
@@ -126,27 +213,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
     float *eG = reinterpret_cast<float *>(sm + kOffEG);
     float *suf = reinterpret_cast<float *>(sm + kOffSuf);
     float *wprod = reinterpret_cast<float *>(sm + kOffWP);
-    int *misc = reinterpret_cast<int *>(sm + kOffMisc);  // slot, base, W, ok, tmem, err
+    int *misc = reinterpret_cast<int *>(sm + kOffMisc);  // [0..3] next unit, [4] tmem, [5] err
     const uint32_t bar_gram = sm_s + kOffBar, bar_s0 = sm_s + kOffBar + 8,
                    bar_p = sm_s + kOffBar + 16, bar_vh = sm_s + kOffBar + 24;
     // v history of this CTA's rows, staged over the dead A matrix: [W][kBV] bf16
     const __nv_bfloat16 *vh = reinterpret_cast<const __nv_bfloat16 *>(sm + kOffA);
 
-    const int hv = blockIdx.x, bb = blockIdx.y, vb = blockIdx.z;
     const int T = P.T, L = P.L, HV = P.HV, H = P.H, V = P.V;
-    const int h = hv / P.G;
+    const int VB = V / kBV;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int v0 = vb * kBV;
+    const __nv_bfloat16 *rawk = reinterpret_cast<const __nv_bfloat16 *>(P.rawk);
+    __nv_bfloat16 *rawk_w = reinterpret_cast<__nv_bfloat16 *>(P.rawk);
+    const __nv_bfloat16 *rawv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv);
+    __nv_bfloat16 *rawv_w = reinterpret_cast<__nv_bfloat16 *>(P.rawv);
 
     if (tid == 0) {
-        int slot = slot_idx[bb], base = 0, W = 0;
-        uint32_t st = 0;
-        const bool ok = row_cursor_ok(C, slot, T, L, &base, &W, &st);
-        if (st && vb == 0 && hv == 0) atomicOr(C.status, st);
-        misc[0] = slot;
-        misc[1] = base;
-        misc[2] = W;
-        misc[3] = ok ? 1 : 0;
         misc[5] = 0;
         ptx::mbar_init(bar_gram, 1);
         ptx::mbar_init(bar_s0, 1);
@@ -154,385 +235,390 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         ptx::mbar_init(bar_vh, 1);
         ptx::mbar_init_fence();
         ptx::prefetch_tmap(&tmap_s0);
-        if (ok) {  // checkpoint tile and v history into L2 now; used at the end
-            const float *s0 = P.checkpoint + (((size_t)slot * HV + hv) * V + v0) * kK;
-            ptx::prefetch_l2(s0, kBV * kK * 4);
-            const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv) +
-                                      ((size_t)slot * HV + hv) * L * V;
-            const int first = (L - base) < W ? (L - base) : W;   // records before the wrap
-            if (first > 0) ptx::prefetch_l2(rv + (size_t)base * V, first * V * 2);
-            if (W > first) ptx::prefetch_l2(rv, (W - first) * V * 2);
-        }
+        fetch_unit(P, C, slot_idx, blockIdx.x, nunits, VB, misc);
     }
     if (warp == 0) ptx::tmem_alloc(sm_s + kOffMisc + 16, kTmemCols);
-    // zero the q_eff operand: rows T..7 must be zero-or-ignored, rows 8..15 get c
+    // zero the q_eff operand: rows T..7 stay zero; rows 8..15 carry c
     for (int i = tid; i < 4 * kQAtom / 16; i += kThreads)
         reinterpret_cast<float4 *>(sm + kOffQ)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = static_cast<uint32_t>(misc[4]);
-    const int slot = misc[0], base = misc[1], W = misc[2];
-    const bool ok = misc[3] != 0;
-    const int n = W + T;
-    const int vrow = v0 + tid;
+    uint32_t ph_gram = 0, ph_s0 = 0, ph_p = 0, ph_vh = 0;   // mbarrier phase bits
 
-    if (ok) {
+    UnitInfo cur{misc[0], misc[1], misc[2], misc[3]};
+    UnitLoads<TM> R;
+    int u = blockIdx.x;
+    if (u < nunits) {
+        const int hv0 = u % HV, rest = u / HV;
+        issue_unit_loads<TM>(P, cur, rest / VB, hv0, rest % VB, tid, q, k, v, a, bgate, A_log, dt_bias, R);
+    }
+
+    for (; u < nunits; u += gridDim.x) {
+        const int hv = u % HV, rest = u / HV, vb = rest % VB, bb = rest / VB;
+        const int un = u + gridDim.x;
+        const int h = hv / P.G;
+        const int v0 = vb * kBV, vrow = v0 + tid;
+        const int slot = cur.slot, base = cur.base, W = cur.W;
+        const bool ok = cur.ok != 0;
+        const int n = W + T;
         const size_t sh_hv = (size_t)slot * HV + hv, sh_h = (size_t)slot * H + h;
-        const __nv_bfloat16 *rawk = reinterpret_cast<const __nv_bfloat16 *>(P.rawk);
-        __nv_bfloat16 *rawk_w = reinterpret_cast<__nv_bfloat16 *>(P.rawk);
-        const __nv_bfloat16 *rawv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv);
-        __nv_bfloat16 *rawv_w = reinterpret_cast<__nv_bfloat16 *>(P.rawv);
         const bool k_writer = (hv % P.G == 0) && vb == 0;
+        bool waited = true;
 
-        // ---- 1. global reads: two threads per token row (keys 0..n-1, then the
-        //         T queries), 128 bytes each as 8 x 16 B; the gate inputs of
-        //         token tid and the window values of state row tid
-        float g_in = 0.f, b_in = 0.f, alog = 0.f, dtb = 0.f;
-        const int pj = ring_pos(base, tid, L);
-        if (tid < W) {
-            g_in = P.ring_g[sh_hv * L + pj];
-            b_in = P.ring_beta[sh_hv * L + pj];
-        } else if (tid < n) {
-            const size_t tok = (size_t)bb * T + (tid - W);
-            g_in = __bfloat162float(a[tok * HV + hv]);
-            b_in = __bfloat162float(bgate[tok * HV + hv]);
-            alog = A_log[hv];
-            dtb = dt_bias[hv];
-        }
-        __nv_bfloat16 vwin_raw[TM];
+        if (ok) {
+            // ---- 1. normalise the token rows (loaded earlier) into X (SW128
+            //         K-major); gates; ring side channel of the window
+            const int half = tid & 1;
+            for (int pass = 0; pass < 2; ++pass) {
+                if (pass == 1 && n + T <= 64) break;  // a second pass only when W > L - 2T
+                const int t = (tid >> 1) + 64 * pass;
+                const bool has_row = t < n + T;
+                if (pass == 1) {  // rows 64.. (rare): load them now
+                    const __nv_bfloat16 *src = q;
+                    if (t < W)
+                        src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
+                    else if (t < n)
+                        src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
+                    else if (has_row)
+                        src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
 #pragma unroll
-        for (int s = 0; s < TM; ++s)
-            vwin_raw[s] = (s < T && vrow < V) ? v[(((size_t)bb * T + s) * HV + hv) * V + vrow]
-                                               : __float2bfloat16_rn(0.0f);
-        const int half = tid & 1;
-        for (int pass = 0; pass < 2; ++pass) {
-            if (pass == 1 && n + T <= 64) break;  // a second pass only when W > L - 2T
-            const int t = (tid >> 1) + 64 * pass;
-            const bool has_row = t < n + T;
-            const __nv_bfloat16 *src = q;
-            if (t < W)
-                src = rawk + (sh_h * L + ring_pos(base, t, L)) * kK;
-            else if (t < n)
-                src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
-            else if (has_row)
-                src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
-            uint4 raw[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                raw[c] = has_row ? reinterpret_cast<const uint4 *>(src)[8 * half + c]
-                                 : make_uint4(0u, 0u, 0u, 0u);
-            float ss[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
-                    ss[e] = fmaf(f.x, f.x, ss[e]);
-                    ss[e] = fmaf(f.y, f.y, ss[e]);
+                    for (int c = 0; c < 8; ++c)
+                        R.raw[c] = has_row ? reinterpret_cast<const uint4 *>(src)[8 * half + c]
+                                           : make_uint4(0u, 0u, 0u, 0u);
                 }
-            }
-            float sq = (ss[0] + ss[1]) + (ss[2] + ss[3]);
-            sq += __shfl_xor_sync(0xffffffffu, sq, 1);   // the row's other half
-            if (has_row) {
-                const float r = 1.0f / sqrtf(sq + P.l2_eps);
-                const int row = t < n ? t : kQRow + (t - n);
+                float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {  // chunk c of this half: k = 64 half + 8c .. + 7
-                    const uint32_t w4[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
-                    float f[8];
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t w4[4] = {R.raw[c].x, R.raw[c].y, R.raw[c].z, R.raw[c].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
-                        f[2 * e] = x.x * r;
-                        f[2 * e + 1] = x.y * r;
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                        ss[e] = fmaf(f.x, f.x, ss[e]);
+                        ss[e] = fmaf(f.y, f.y, ss[e]);
                     }
-                    const int k0 = 64 * half + 8 * c;
-                    *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, k0)) =
-                        make_float4(f[0], f[1], f[2], f[3]);
-                    *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, k0 + 4)) =
-                        make_float4(f[4], f[5], f[6], f[7]);
                 }
-                if (t >= W && t < n && k_writer) {  // side channel: raw key, bitwise
-                    uint4 *dst = reinterpret_cast<uint4 *>(rawk_w + (sh_h * L + ring_pos(base, t, L)) * kK);
+                float sq = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+                sq += __shfl_xor_sync(0xffffffffu, sq, 1);   // the row's other half
+                if (has_row) {
+                    const float r = 1.0f / sqrtf(sq + P.l2_eps);
+                    const int row = t < n ? t : kQRow + (t - n);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) dst[8 * half + c] = raw[c];
+                    for (int c = 0; c < 8; ++c) {  // chunk c of this half: k = 64 half + 8c .. + 7
+                        const uint32_t w4[4] = {R.raw[c].x, R.raw[c].y, R.raw[c].z, R.raw[c].w};
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                            f[2 * e] = x.x * r;
+                            f[2 * e + 1] = x.y * r;
+                        }
+                        const int k0 = 64 * half + 8 * c;
+                        *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, k0)) =
+                            make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<float4 *>(sm + kOffX + sw128(kXAtom, row, k0 + 4)) =
+                            make_float4(f[4], f[5], f[6], f[7]);
+                    }
+                    if (t >= W && t < n && k_writer) {  // side channel: raw key, bitwise
+                        uint4 *dst = reinterpret_cast<uint4 *>(rawk_w + (sh_h * L + ring_pos(base, t, L)) * kK);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) dst[8 * half + c] = R.raw[c];
+                    }
                 }
             }
-        }
-        if (tid < n) {
-            float g = g_in, be = b_in;
-            if (tid >= W) {
-                g = gate_g(alog, g_in, dtb);
-                be = gate_beta(b_in);
-                if (vb == 0) {
-                    P.ring_g[sh_hv * L + pj] = g;
-                    P.ring_beta[sh_hv * L + pj] = be;
+            if (tid < n) {
+                const int pj = ring_pos(base, tid, L);
+                float g = R.g_in, be = R.b_in;
+                if (tid >= W) {
+                    g = gate_g(R.alog, R.g_in, R.dtb);
+                    be = gate_beta(R.b_in);
+                    if (vb == 0) {
+                        P.ring_g[sh_hv * L + pj] = g;
+                        P.ring_beta[sh_hv * L + pj] = be;
+                    }
                 }
+                alpha[tid] = expf(g);
+                betaS[tid] = be;
             }
-            alpha[tid] = expf(g);
-            betaS[tid] = be;
-        }
-#pragma unroll
-        for (int s = 0; s < TM; ++s)
-            if (s < T && vrow < V) rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = vwin_raw[s];
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- 2. Gram on the tensor core (D[i, j] = <X_i, X_j>, M = 128, N = 80),
-        //         decay products on CUDA cores meanwhile
-        if (tid == 0) {
-            ptx::tc_fence_after_sync();
-            constexpr uint32_t idesc = ptx::idesc_tf32(128, kXRows);
-#pragma unroll
-            for (int kb = 0; kb < 4; ++kb)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t d = ptx::smem_desc_sw128(sm_s + kOffX + kb * kXAtom + ks * 32);
-                    ptx::mma_tf32(tmem + kGramCol, d, d, idesc, (kb | ks) != 0);
-                }
-            ptx::mma_commit(bar_gram);
-        }
-        if (warp == 1) {  // eG_j = prod_{t <= j} alpha_t, j < n
-            const float a0 = 2 * lane < n ? alpha[2 * lane] : 1.0f;
-            const float a1 = 2 * lane + 1 < n ? alpha[2 * lane + 1] : 1.0f;
-            const float incl = warp_prefix_prod(a0 * a1, lane);
-            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 1.0f;
-            eG[2 * lane] = excl * a0;
-            eG[2 * lane + 1] = incl;
-        } else if (warp == 2) {  // suf[t] = prod_{u=t}^{W-1} alpha_u, t <= W (suf[W] = 1)
-            const int u0 = 2 * lane, u1 = 2 * lane + 1;  // reversed index u = W-1-t
-            const float a0 = u0 < W ? alpha[W - 1 - u0] : 1.0f;
-            const float a1 = u1 < W ? alpha[W - 1 - u1] : 1.0f;
-            const float incl = warp_prefix_prod(a0 * a1, lane);
-            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 1.0f;
-            if (u0 < W) suf[W - 1 - u0] = excl * a0;
-            if (u1 < W) suf[W - 1 - u1] = incl;
-            if (lane == 0) suf[W] = 1.0f;
-        } else if (warp == 3 && lane == 0) {  // wprod[s] = prod_{t=W}^{W+s} alpha_t
-            float c = 1.0f;
 #pragma unroll
             for (int s = 0; s < TM; ++s)
-                if (s < T) {
-                    c *= alpha[W + s];
-                    wprod[s] = c;
-                }
-        }
-        __syncthreads();
-        bool waited = ptx::mbar_wait(bar_gram, 0);
-        ptx::tc_fence_after_sync();
+                if (s < T && vrow < V) rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = R.vwin[s];
+            ptx::fence_proxy_async_smem();
+            __syncthreads();
 
-        // ---- 3. per token i (thread i): row i of A (zero above the diagonal), row i of F
-        {
-            const int i = tid;
-            const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + kGramCol;
-            // tcgen05.ld is warp-collective: every load below runs on all lanes
-            float gq[16];
-            ptx::tmem_ld16(tbase + kQRow, gq);   // columns 64..79: the query columns
-            ptx::tmem_ld_wait();
-            const bool row_live = i < n;
-            const float bi = row_live ? betaS[i] : 0.0f;
-            float c = 1.0f;
-#pragma unroll 1
-            for (int cc = kLMax / 16 - 1; cc >= 0; --cc) {  // key columns, high chunk first
-                float gk[16];
-                ptx::tmem_ld16(tbase + 16 * cc, gk);
-                ptx::tmem_ld_wait();
-                if (row_live) {
-                    float val[16];
+            // ---- 2. Gram on the tensor core (D[i, j] = <X_i, X_j>, M = 128, N = 80),
+            //         decay products on CUDA cores meanwhile
+            if (tid == 0) {
+                ptx::tc_fence_after_sync();
+                constexpr uint32_t idesc = ptx::idesc_tf32(128, kXRows);
 #pragma unroll
-                    for (int x = 15; x >= 0; --x) {
-                        const int r = 16 * cc + x;
-                        val[x] = 0.0f;
-                        if (r < i) {
-                            c *= alpha[r + 1];               // Gamma(i, r)
-                            val[x] = bi * c * gk[x];
-                        }
+                for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t d = ptx::smem_desc_sw128(sm_s + kOffX + kb * kXAtom + ks * 32);
+                        ptx::mma_tf32(tmem + kGramCol, d, d, idesc, (kb | ks) != 0);
                     }
-#pragma unroll
-                    for (int x = 0; x < 16; x += 4)
-                        *reinterpret_cast<float4 *>(A + i * kALd + 16 * cc + x) =
-                            make_float4(val[x], val[x + 1], val[x + 2], val[x + 3]);
-                }
+                ptx::mma_commit(bar_gram);
             }
-            if (row_live) {
-                // Gamma(W+s, i): products of the suffix and window decays
-                const float si = i < W ? suf[i + 1] : 1.0f;
-                float cw = 1.0f;
-                float fr[TM];
+            if (warp == 1) {  // eG_j = prod_{t <= j} alpha_t, j < n
+                const float a0 = 2 * lane < n ? alpha[2 * lane] : 1.0f;
+                const float a1 = 2 * lane + 1 < n ? alpha[2 * lane + 1] : 1.0f;
+                const float incl = warp_prefix_prod(a0 * a1, lane);
+                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+                if (lane == 0) excl = 1.0f;
+                eG[2 * lane] = excl * a0;
+                eG[2 * lane + 1] = incl;
+            } else if (warp == 2) {  // suf[t] = prod_{u=t}^{W-1} alpha_u, t <= W (suf[W] = 1)
+                const int u0 = 2 * lane, u1 = 2 * lane + 1;  // reversed index u = W-1-t
+                const float a0 = u0 < W ? alpha[W - 1 - u0] : 1.0f;
+                const float a1 = u1 < W ? alpha[W - 1 - u1] : 1.0f;
+                const float incl = warp_prefix_prod(a0 * a1, lane);
+                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+                if (lane == 0) excl = 1.0f;
+                if (u0 < W) suf[W - 1 - u0] = excl * a0;
+                if (u1 < W) suf[W - 1 - u1] = incl;
+                if (lane == 0) suf[W] = 1.0f;
+            } else if (warp == 3 && lane == 0) {  // wprod[s] = prod_{t=W}^{W+s} alpha_t
+                float c = 1.0f;
 #pragma unroll
-                for (int s = 0; s < TM; ++s) {
-                    float f = 0.0f;
+                for (int s = 0; s < TM; ++s)
                     if (s < T) {
-                        const int t = W + s;
-                        if (i < W) {
-                            f = si * wprod[s] * gq[s];
-                        } else if (t >= i) {
-                            if (t > i) cw *= alpha[t];
-                            f = cw * gq[s];
-                        }
+                        c *= alpha[W + s];
+                        wprod[s] = c;
                     }
-                    fr[s] = f;
-                }
-#pragma unroll
-                for (int s = 0; s < TM; s += 4)
-                    *reinterpret_cast<float4 *>(F + i * TM + s) = make_float4(fr[s], fr[s + 1], fr[s + 2], fr[s + 3]);
             }
-        }
-        if (!waited && tid == 0) misc[5] = 1;
-        __syncthreads();
+            __syncthreads();
+            waited = ptx::mbar_wait(bar_gram, ph_gram);
+            ph_gram ^= 1u;
+            ptx::tc_fence_after_sync();
 
-        // ---- 4. M (I + A) = F^T, all T rows in warp 0; lane l ends with M[s][l], M[s][l+32]
-        if (warp == 0) {
-            float f0[TM], f1[TM];
+            // ---- 3. per token i (thread i): row i of A (zero above the diagonal), row i of F
+            {
+                const int i = tid;
+                const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + kGramCol;
+                // tcgen05.ld is warp-collective: every load below runs on all lanes
+                float gq[16];
+                ptx::tmem_ld16(tbase + kQRow, gq);   // columns 64..79: the query columns
+                ptx::tmem_ld_wait();
+                const bool row_live = i < n;
+                const float bi = row_live ? betaS[i] : 0.0f;
+                float c = 1.0f;
+#pragma unroll 1
+                for (int cc = kLMax / 16 - 1; cc >= 0; --cc) {  // key columns, high chunk first
+                    float gk[16];
+                    ptx::tmem_ld16(tbase + 16 * cc, gk);
+                    ptx::tmem_ld_wait();
+                    if (row_live) {
+                        float val[16];
 #pragma unroll
-            for (int s = 0; s < TM; ++s) {
-                f0[s] = lane < n ? F[lane * TM + s] : 0.0f;
-                f1[s] = lane + 32 < n ? F[(lane + 32) * TM + s] : 0.0f;
-            }
-            // four tokens j-3..j per step: the 4 x 4 diagonal block is solved
-            // redundantly on every lane, then all lanes apply the four updates
-            // (which also leave f[j-3..j] equal to their final values)
-            int j = n - 1;
-            for (; j >= 3; j -= 4) {
-                float a[4][2], d[6];
+                        for (int x = 15; x >= 0; --x) {
+                            const int r = 16 * cc + x;
+                            val[x] = 0.0f;
+                            if (r < i) {
+                                c *= alpha[r + 1];               // Gamma(i, r)
+                                val[x] = bi * c * gk[x];
+                            }
+                        }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    a[q][0] = A[(j - q) * kALd + lane];
-                    a[q][1] = A[(j - q) * kALd + 32 + lane];
+                        for (int x = 0; x < 16; x += 4)
+                            *reinterpret_cast<float4 *>(A + i * kALd + 16 * cc + x) =
+                                make_float4(val[x], val[x + 1], val[x + 2], val[x + 3]);
+                    }
                 }
-                d[0] = A[j * kALd + j - 1];        // A[j][j-1]
-                d[1] = A[j * kALd + j - 2];        // A[j][j-2]
-                d[2] = A[j * kALd + j - 3];        // A[j][j-3]
-                d[3] = A[(j - 1) * kALd + j - 2];  // A[j-1][j-2]
-                d[4] = A[(j - 1) * kALd + j - 3];  // A[j-1][j-3]
-                d[5] = A[(j - 2) * kALd + j - 3];  // A[j-2][j-3]
+                if (row_live) {
+                    // Gamma(W+s, i): products of the suffix and window decays
+                    const float si = i < W ? suf[i + 1] : 1.0f;
+                    float cw = 1.0f;
+                    float fr[TM];
 #pragma unroll
-                for (int s = 0; s < TM; ++s) {
-                    float fj[4];
+                    for (int s = 0; s < TM; ++s) {
+                        float f = 0.0f;
+                        if (s < T) {
+                            const int t = W + s;
+                            if (i < W) {
+                                f = si * wprod[s] * gq[s];
+                            } else if (t >= i) {
+                                if (t > i) cw *= alpha[t];
+                                f = cw * gq[s];
+                            }
+                        }
+                        fr[s] = f;
+                    }
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        fj[q] = __shfl_sync(0xffffffffu, (j - q) < 32 ? f0[s] : f1[s], (j - q) & 31);
-                    const float m0 = fj[0];
-                    const float m1 = fmaf(-d[0], m0, fj[1]);
-                    const float m2 = fmaf(-d[3], m1, fmaf(-d[1], m0, fj[2]));
-                    const float m3 = fmaf(-d[5], m2, fmaf(-d[4], m1, fmaf(-d[2], m0, fj[3])));
-                    f0[s] = fmaf(-a[3][0], m3, fmaf(-a[2][0], m2, fmaf(-a[1][0], m1, fmaf(-a[0][0], m0, f0[s]))));
-                    f1[s] = fmaf(-a[3][1], m3, fmaf(-a[2][1], m2, fmaf(-a[1][1], m1, fmaf(-a[0][1], m0, f1[s]))));
-                }
-            }
-            for (; j >= 0; --j) {
-                const float a0 = A[j * kALd + lane], a1 = A[j * kALd + 32 + lane];
-#pragma unroll
-                for (int s = 0; s < TM; ++s) {
-                    const float m = __shfl_sync(0xffffffffu, j < 32 ? f0[s] : f1[s], j & 31);
-                    f0[s] = fmaf(-a0, m, f0[s]);
-                    f1[s] = fmaf(-a1, m, f1[s]);
-                }
-            }
-            // c = M beta (output) and c eG (effective query), rows j = lane, lane + 32
-#pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                const int j = lane + 32 * hlf;
-                const float bj = j < n ? betaS[j] : 0.0f, ej = j < n ? eG[j] : 0.0f;
-                float cj[TM], ce[TM];
-#pragma unroll
-                for (int s = 0; s < TM; ++s) {
-                    cj[s] = (hlf ? f1[s] : f0[s]) * bj;
-                    ce[s] = cj[s] * ej;
-                }
-#pragma unroll
-                for (int s = 0; s < TM; s += 4) {
-                    *reinterpret_cast<float4 *>(sm + c_off(j) + 4 * s) =
-                        make_float4(cj[s], cj[s + 1], cj[s + 2], cj[s + 3]);
-                    *reinterpret_cast<float4 *>(F + j * TM + s) =
-                        make_float4(ce[s], ce[s + 1], ce[s + 2], ce[s + 3]);
+                    for (int s = 0; s < TM; s += 4)
+                        *reinterpret_cast<float4 *>(F + i * TM + s) =
+                            make_float4(fr[s], fr[s + 1], fr[s + 2], fr[s + 3]);
                 }
             }
-        }
-        __syncthreads();
+            if (!waited && tid == 0) misc[5] = 1;
+            __syncthreads();
 
-        // ---- 5a. the v history of this CTA's rows into the (now dead) A
-        //          matrix: one 1-D bulk copy per record, spread over warp 0
-        if (warp == 0) {
-            ptx::fence_proxy_async_smem();   // the A matrix was last read by generic loads
-            if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)W * kBV * 2);
-            __syncwarp();
-            for (int j = lane; j < W; j += 32)
-                ptx::bulk_copy_g2s(sm_s + kOffA + j * kBV * 2,
-                                   rawv + (sh_hv * L + ring_pos(base, j, L)) * V + v0, kBV * 2,
-                                   bar_vh);
-        }
-        // ---- 5. q_eff (thread = key channel): eG_{W+s} q^_s - sum_j c[j][s] eG_j k^_j
-        {
-            const int kk = tid;
-            const int katom = kk >> 5, kbyte = (kk & 31) * 4, kch = kbyte >> 4;
-            const uint32_t xbase = kOffX + katom * kXAtom + (kbyte & 15);
-            float acc[TM];
+            // ---- 4. M (I + A) = F^T, all T rows in warp 0; lane l ends with M[s][l],
+            //         M[s][l+32].  Meanwhile one thread of warp 1 fetches the next unit.
+            if (warp == 0) {
+                float f0[TM], f1[TM];
 #pragma unroll
-            for (int s = 0; s < TM; ++s) acc[s] = 0.0f;
-            for (int j = 0; j < n; ++j) {
-                const float x = *reinterpret_cast<const float *>(sm + xbase + j * 128 + ((kch ^ (j & 7)) << 4));
-#pragma unroll
-                for (int s = 0; s < TM; s += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(F + j * TM + s);
-                    acc[s] = fmaf(-c4.x, x, acc[s]);
-                    acc[s + 1] = fmaf(-c4.y, x, acc[s + 1]);
-                    acc[s + 2] = fmaf(-c4.z, x, acc[s + 2]);
-                    acc[s + 3] = fmaf(-c4.w, x, acc[s + 3]);
+                for (int s = 0; s < TM; ++s) {
+                    f0[s] = lane < n ? F[lane * TM + s] : 0.0f;
+                    f1[s] = lane + 32 < n ? F[(lane + 32) * TM + s] : 0.0f;
                 }
+                // four tokens j-3..j per step: the 4 x 4 diagonal block is solved
+                // redundantly on every lane, then all lanes apply the four updates
+                // (which also leave f[j-3..j] equal to their final values)
+                int j = n - 1;
+                for (; j >= 3; j -= 4) {
+                    float ar[4][2], d[6];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        ar[qq][0] = A[(j - qq) * kALd + lane];
+                        ar[qq][1] = A[(j - qq) * kALd + 32 + lane];
+                    }
+                    d[0] = A[j * kALd + j - 1];        // A[j][j-1]
+                    d[1] = A[j * kALd + j - 2];        // A[j][j-2]
+                    d[2] = A[j * kALd + j - 3];        // A[j][j-3]
+                    d[3] = A[(j - 1) * kALd + j - 2];  // A[j-1][j-2]
+                    d[4] = A[(j - 1) * kALd + j - 3];  // A[j-1][j-3]
+                    d[5] = A[(j - 2) * kALd + j - 3];  // A[j-2][j-3]
+#pragma unroll
+                    for (int s = 0; s < TM; ++s) {
+                        float fj[4];
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            fj[qq] = __shfl_sync(0xffffffffu, (j - qq) < 32 ? f0[s] : f1[s], (j - qq) & 31);
+                        const float m0 = fj[0];
+                        const float m1 = fmaf(-d[0], m0, fj[1]);
+                        const float m2 = fmaf(-d[3], m1, fmaf(-d[1], m0, fj[2]));
+                        const float m3 = fmaf(-d[5], m2, fmaf(-d[4], m1, fmaf(-d[2], m0, fj[3])));
+                        f0[s] = fmaf(-ar[3][0], m3, fmaf(-ar[2][0], m2, fmaf(-ar[1][0], m1, fmaf(-ar[0][0], m0, f0[s]))));
+                        f1[s] = fmaf(-ar[3][1], m3, fmaf(-ar[2][1], m2, fmaf(-ar[1][1], m1, fmaf(-ar[0][1], m0, f1[s]))));
+                    }
+                }
+                for (; j >= 0; --j) {
+                    const float a0 = A[j * kALd + lane], a1 = A[j * kALd + 32 + lane];
+#pragma unroll
+                    for (int s = 0; s < TM; ++s) {
+                        const float m = __shfl_sync(0xffffffffu, j < 32 ? f0[s] : f1[s], j & 31);
+                        f0[s] = fmaf(-a0, m, f0[s]);
+                        f1[s] = fmaf(-a1, m, f1[s]);
+                    }
+                }
+                // c = M beta (output) and c eG (effective query), rows j = lane, lane + 32
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int jj = lane + 32 * hlf;
+                    const float bj = jj < n ? betaS[jj] : 0.0f, ej = jj < n ? eG[jj] : 0.0f;
+                    float cj[TM], ce[TM];
+#pragma unroll
+                    for (int s = 0; s < TM; ++s) {
+                        cj[s] = (hlf ? f1[s] : f0[s]) * bj;
+                        ce[s] = cj[s] * ej;
+                    }
+#pragma unroll
+                    for (int s = 0; s < TM; s += 4) {
+                        *reinterpret_cast<float4 *>(sm + c_off(jj) + 4 * s) =
+                            make_float4(cj[s], cj[s + 1], cj[s + 2], cj[s + 3]);
+                        *reinterpret_cast<float4 *>(F + jj * TM + s) =
+                            make_float4(ce[s], ce[s + 1], ce[s + 2], ce[s + 3]);
+                    }
+                }
+            } else if (tid == 32) {
+                fetch_unit(P, C, slot_idx, un, nunits, VB, misc);
             }
+            __syncthreads();
+
+            // ---- 5. the v history of this CTA's rows into the (now dead) A
+            //         matrix: one 1-D bulk copy per record, spread over warp 0
+            if (warp == 0 && W > 0) {
+                ptx::fence_proxy_async_smem();   // the A matrix was last read by generic loads
+                if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)W * kBV * 2);
+                __syncwarp();
+                for (int jj = lane; jj < W; jj += 32)
+                    ptx::bulk_copy_g2s(sm_s + kOffA + jj * kBV * 2,
+                                       rawv + (sh_hv * L + ring_pos(base, jj, L)) * V + v0, kBV * 2,
+                                       bar_vh);
+            }
+            // q_eff (thread = key channel): eG_{W+s} q^_s - sum_j c[j][s] eG_j k^_j
+            {
+                const int kk = tid;
+                const int katom = kk >> 5, kbyte = (kk & 31) * 4, kch = kbyte >> 4;
+                const uint32_t xbase = kOffX + katom * kXAtom + (kbyte & 15);
+                float acc[TM];
 #pragma unroll
-            for (int s = 0; s < TM; ++s)
-                if (s < T)
-                    acc[s] += eG[W + s] * *reinterpret_cast<const float *>(
-                                              sm + xbase + (kQRow + s) * 128 + ((kch ^ ((kQRow + s) & 7)) << 4));
+                for (int s = 0; s < TM; ++s) acc[s] = 0.0f;
+                for (int j = 0; j < n; ++j) {
+                    const float x = *reinterpret_cast<const float *>(sm + xbase + j * 128 + ((kch ^ (j & 7)) << 4));
 #pragma unroll
-            for (int s = 0; s < TM; ++s)
-                if (s < T) *reinterpret_cast<float *>(sm + kOffQ + sw128(kQAtom, s, kk)) = acc[s];
+                    for (int s = 0; s < TM; s += 4) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(F + j * TM + s);
+                        acc[s] = fmaf(-c4.x, x, acc[s]);
+                        acc[s + 1] = fmaf(-c4.y, x, acc[s + 1]);
+                        acc[s + 2] = fmaf(-c4.z, x, acc[s + 2]);
+                        acc[s + 3] = fmaf(-c4.w, x, acc[s + 3]);
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < TM; ++s)
+                    if (s < T)
+                        acc[s] += eG[W + s] * *reinterpret_cast<const float *>(
+                                                  sm + xbase + (kQRow + s) * 128 + ((kch ^ ((kQRow + s) & 7)) << 4));
+#pragma unroll
+                for (int s = 0; s < TM; ++s)
+                    if (s < T) *reinterpret_cast<float *>(sm + kOffQ + sw128(kQAtom, s, kk)) = acc[s];
+            }
+        } else {
+            if (tid == 0) fetch_unit(P, C, slot_idx, un, nunits, VB, misc);
+            if (vrow < V)
+                for (int s = 0; s < T; ++s)
+                    out[(((size_t)bb * T + s) * HV + hv) * V + vrow] = __float2bfloat16_rn(0.0f);
         }
+
         // output part that does not need the checkpoint: sum_j c[j][s] v_j,
         // from the staged v history and the window values
         float vt[TM];
 #pragma unroll
         for (int s = 0; s < TM; ++s) vt[s] = 0.0f;
-        bool vh_ok = W == 0 || ptx::mbar_wait(bar_vh, 0);
-        if (vrow < V) {
-            for (int j = 0; j < W; ++j) {
-                const float x = __bfloat162float(vh[j * kBV + tid]);
-#pragma unroll
-                for (int s = 0; s < TM; s += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(j) + 4 * s);
-                    vt[s] = fmaf(c4.x, x, vt[s]);
-                    vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
-                    vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
-                    vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
-                }
+        if (ok) {
+            bool vh_ok = true;
+            if (W > 0) {
+                vh_ok = ptx::mbar_wait(bar_vh, ph_vh);
+                ph_vh ^= 1u;
             }
-#pragma unroll
-            for (int s2 = 0; s2 < TM; ++s2) {
-                if (s2 < T) {
-                    const float x = __bfloat162float(vwin_raw[s2]);
+            if (vrow < V) {
+                for (int j = 0; j < W; ++j) {
+                    const float x = __bfloat162float(vh[j * kBV + tid]);
 #pragma unroll
                     for (int s = 0; s < TM; s += 4) {
-                        const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(W + s2) + 4 * s);
+                        const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(j) + 4 * s);
                         vt[s] = fmaf(c4.x, x, vt[s]);
                         vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
                         vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
                         vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
                     }
                 }
+#pragma unroll
+                for (int s2 = 0; s2 < TM; ++s2) {
+                    if (s2 < T) {
+                        const float x = __bfloat162float(R.vwin[s2]);
+#pragma unroll
+                        for (int s = 0; s < TM; s += 4) {
+                            const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(W + s2) + 4 * s);
+                            vt[s] = fmaf(c4.x, x, vt[s]);
+                            vt[s + 1] = fmaf(c4.y, x, vt[s + 1]);
+                            vt[s + 2] = fmaf(c4.z, x, vt[s + 2]);
+                            vt[s + 3] = fmaf(c4.w, x, vt[s + 3]);
+                        }
+                    }
+                }
             }
+            if (!vh_ok && tid == 0) misc[5] = 1;
+            ptx::fence_proxy_async_smem();
         }
-        if (!vh_ok && tid == 0) misc[5] = 1;
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
+        __syncthreads();   // next unit's cursors visible; R0 free for the checkpoint tile
 
-        // ---- 6. checkpoint tile by TMA (over the dead key buffers), then P = S0 q_eff^T
-        if (tid == 0) {
+        // ---- 6. checkpoint tile by TMA (over the dead key buffers); the next
+        //         unit's loads go out while it is in flight; then P = S0 q_eff^T
+        if (ok && tid == 0) {
             ptx::fence_proxy_async_smem();
             ptx::mbar_expect_tx(bar_s0, kR0Bytes);
             const int32_t y = (int32_t)((sh_hv * V) + v0);
@@ -540,40 +626,52 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             for (int kb = 0; kb < 4; ++kb)
                 ptx::tma_load_2d(sm_s + kOffS0 + kb * kS0Atom, &tmap_s0, bar_s0, kb * 32, y);
         }
-        waited = ptx::mbar_wait(bar_s0, 0);
-        if (tid == 0) {
-            if (!waited) {
-                misc[5] = 1;
-            } else {
-                ptx::tc_fence_after_sync();
-                constexpr uint32_t idesc = ptx::idesc_tf32(128, 16);
+        const UnitInfo nxt{misc[0], misc[1], misc[2], misc[3]};
+        if (un < nunits) {
+            const int hvn = un % HV, restn = un / HV;
+            issue_unit_loads<TM>(P, nxt, restn / VB, hvn, restn % VB, tid, q, k, v, a, bgate, A_log,
+                                 dt_bias, R);
+        }
+        if (ok) {
+            waited = ptx::mbar_wait(bar_s0, ph_s0);
+            ph_s0 ^= 1u;
+            if (tid == 0) {
+                if (!waited) {
+                    misc[5] = 1;
+                } else {
+                    ptx::tc_fence_after_sync();
+                    constexpr uint32_t idesc = ptx::idesc_tf32(128, 16);
 #pragma unroll
-                for (int kb = 0; kb < 4; ++kb)
+                    for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        ptx::mma_tf32(tmem + kPCol,
-                                      ptx::smem_desc_sw128(sm_s + kOffS0 + kb * kS0Atom + ks * 32),
-                                      ptx::smem_desc_sw128(sm_s + kOffQ + kb * kQAtom + ks * 32),
-                                      idesc, (kb | ks) != 0);
+                        for (int ks = 0; ks < 4; ++ks)
+                            ptx::mma_tf32(tmem + kPCol,
+                                          ptx::smem_desc_sw128(sm_s + kOffS0 + kb * kS0Atom + ks * 32),
+                                          ptx::smem_desc_sw128(sm_s + kOffQ + kb * kQAtom + ks * 32),
+                                          idesc, (kb | ks) != 0);
+                }
+                ptx::mma_commit(bar_p);
             }
-            ptx::mma_commit(bar_p);
-        }
-        waited = ptx::mbar_wait(bar_p, 0) && waited;
-        ptx::tc_fence_after_sync();
-        float pr[16];
-        ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + kPCol, pr);
-        ptx::tmem_ld_wait();
-        if (!waited) misc[5] = 1;
-        if (vrow < V) {
+            waited = ptx::mbar_wait(bar_p, ph_p) && waited;
+            ph_p ^= 1u;
+            ptx::tc_fence_after_sync();
+            float pr[16];
+            ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + kPCol, pr);
+            ptx::tmem_ld_wait();
+            if (!waited) misc[5] = 1;
+            if (vrow < V) {
 #pragma unroll
-            for (int s = 0; s < TM; ++s)
-                if (s < T)
-                    out[(((size_t)bb * T + s) * HV + hv) * V + vrow] =
-                        __float2bfloat16_rn(P.scale * (pr[s] + vt[s]));
+                for (int s = 0; s < TM; ++s)
+                    if (s < T)
+                        out[(((size_t)bb * T + s) * HV + hv) * V + vrow] =
+                            __float2bfloat16_rn(P.scale * (pr[s] + vt[s]));
+            }
         }
-    } else if (vrow < V) {
-        for (int s = 0; s < T; ++s)
-            out[(((size_t)bb * T + s) * HV + hv) * V + vrow] = __float2bfloat16_rn(0.0f);
+        cur = nxt;
+        // the tile and TMEM columns are reused by the next unit
+        ptx::tc_fence_before_sync();
+        __syncthreads();
+        ptx::tc_fence_after_sync();
     }
 
     // ---- teardown: every TMEM read is complete; free the columns
@@ -622,9 +720,17 @@ cudaError_t launch_tm(const CUtensorMap &tmap, const LayerArgs &P, const CursorA
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(P.HV, B, P.V / tc::kBV);
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, tc::kThreads,
+                                                           tc::kSmemBytes)) != cudaSuccess)
+        return e;
+    const int nunits = B * P.HV * (P.V / tc::kBV);
+    int grid = sms * (per_sm > 0 ? per_sm : 1);
+    if (grid > nunits) grid = nunits;
     kern<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(
-        tmap, P, C, slot_idx, static_cast<const __nv_bfloat16 *>(q),
+        tmap, P, C, slot_idx, nunits, static_cast<const __nv_bfloat16 *>(q),
         static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
         static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), A_log, dt_bias,
         static_cast<__nv_bfloat16 *>(out));
