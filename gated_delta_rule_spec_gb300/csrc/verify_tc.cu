@@ -82,6 +82,11 @@ static_assert(3 * kXAtom + 128 * 128 <= kR0Bytes, "Gram operand overrun leaves R
 static_assert(3 * (kSmemBytes + 1024) <= 228 * 1024, "three CTAs per SM");
 
 constexpr uint32_t kTmemCols = 128;
+// CTAs per SM the kernel is built for: the register cap of the launch bounds
+// (65536 / (3 * 128) = 170 per thread) and three TMEM allocations of 128 of
+// the SM's 512 columns
+constexpr int kCtasPerSm = 3;
+static_assert(kCtasPerSm * kTmemCols <= 512, "TMEM columns of the resident CTAs");
 constexpr uint32_t kGramCol = 0;
 constexpr uint32_t kPCol = 96;
 
@@ -108,34 +113,69 @@ __device__ __forceinline__ float warp_prefix_prod(float x, int lane) {
 
 // One unit = (batch row, v-head, block of 128 state rows).  Fetching a unit
 // means reading its slot and cursors (one thread) and prefetching its
-// checkpoint tile and v history into L2.
+// checkpoint tile and v history into L2.  Inside the unit loop the fetch of
+// the next unit is split into stages spread over the current unit, so that no
+// stage waits on a load: the slot index, then the cursors, then the checks,
+// the prefetch and the hand-over through shared memory.
 struct UnitInfo {
     int slot, base, W, ok;
 };
 
-__device__ __forceinline__ void fetch_unit(const LayerArgs &P, const CursorArgs &C,
-                                           const int32_t *slot_idx, int u, int nunits, int VB,
-                                           int *dst) {
+__device__ __forceinline__ void unit_coords(int u, int HV, int VB, int &bb, int &hv, int &vb) {
+    hv = u % HV;
+    const int rest = u / HV;
+    vb = rest % VB;
+    bb = rest / VB;
+}
+
+// Last stage: checks (status bits as row_cursor_ok sets them), L2 prefetch,
+// hand-over to dst[0..3].  wp and cbase are only read when the slot is in range.
+__device__ __forceinline__ void finish_fetch(const LayerArgs &P, const CursorArgs &C, int u,
+                                             int nunits, int VB, int slot, int wp, int cbase,
+                                             int *dst) {
     if (u >= nunits) {
         dst[0] = -1; dst[1] = 0; dst[2] = 0; dst[3] = 0;
         return;
     }
-    const int hv = u % P.HV, rest = u / P.HV, vb = rest % VB, bb = rest / VB;
-    int slot = slot_idx[bb], base = 0, W = 0;
+    int bb, hv, vb;
+    unit_coords(u, P.HV, VB, bb, hv, vb);
     uint32_t st = 0;
-    const bool ok = row_cursor_ok(C, slot, P.T, P.L, &base, &W, &st);
+    bool ok = false;
+    if (slot >= C.num_slots) st = GDN_SPEC_ST_SLOT_OOR;
+    else if (slot >= 0) {
+        if (wp < 0 || wp > P.L || cbase < 0 || cbase >= P.L) st = GDN_SPEC_ST_CURSOR_CORRUPT;
+        else if (wp + P.T > P.L) st = GDN_SPEC_ST_RING_OVERFLOW;
+        else ok = true;
+    }
     if (st && vb == 0 && hv == 0) atomicOr(C.status, st);
     if (ok) {  // checkpoint tile and v history into L2; used at the end of the unit
         const size_t sh_hv = (size_t)slot * P.HV + hv;
         ptx::prefetch_l2(P.checkpoint + (sh_hv * P.V + vb * kBV) * kK, kBV * kK * 4);
         const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv) + sh_hv * P.L * P.V;
         if (P.V == kBV) {  // whole records are contiguous: one or two segments
-            const int first = (P.L - base) < W ? (P.L - base) : W;
-            if (first > 0) ptx::prefetch_l2(rv + (size_t)base * P.V, first * P.V * 2);
-            if (W > first) ptx::prefetch_l2(rv, (W - first) * P.V * 2);
+            const int first = (P.L - cbase) < wp ? (P.L - cbase) : wp;
+            if (first > 0) ptx::prefetch_l2(rv + (size_t)cbase * P.V, first * P.V * 2);
+            if (wp > first) ptx::prefetch_l2(rv, (wp - first) * P.V * 2);
         }
     }
-    dst[0] = slot; dst[1] = base; dst[2] = W; dst[3] = ok ? 1 : 0;
+    dst[0] = slot; dst[1] = ok ? cbase : 0; dst[2] = ok ? wp : 0; dst[3] = ok ? 1 : 0;
+}
+
+// All stages at once (start-up, and units that have no work to hide it behind).
+__device__ __forceinline__ void fetch_unit(const LayerArgs &P, const CursorArgs &C,
+                                           const int32_t *slot_idx, int u, int nunits, int VB,
+                                           int *dst) {
+    int slot = -1, wp = 0, cbase = 0;
+    if (u < nunits) {
+        int bb, hv, vb;
+        unit_coords(u, P.HV, VB, bb, hv, vb);
+        slot = slot_idx[bb];
+        if (slot >= 0 && slot < C.num_slots) {
+            wp = C.write_pos[slot];
+            cbase = C.cache_base[slot];
+        }
+    }
+    finish_fetch(P, C, u, nunits, VB, slot, wp, cbase, dst);
 }
 
 // The early global reads of a unit, held in registers until its first phase:
@@ -168,9 +208,15 @@ __device__ __forceinline__ void issue_unit_loads(
         src = k + (((size_t)bb * T + (t - W)) * H + h) * kK;
     else if (has_row)
         src = q + (((size_t)bb * T + (t - n)) * H + h) * kK;
+    // zero first, then guarded loads: nothing here reads a loaded register, so
+    // the loads stay in flight until the unit's first phase uses them
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-        R.raw[c] = has_row ? reinterpret_cast<const uint4 *>(src)[8 * half + c] : make_uint4(0u, 0u, 0u, 0u);
+    for (int c = 0; c < 8; ++c) R.raw[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (has_row) {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src) + 8 * half;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) R.raw[c] = s4[c];
+    }
     R.g_in = R.b_in = R.alog = R.dtb = 0.0f;
     if (U.ok && tid < W) {
         const int pj = ring_pos(base, tid, L);
@@ -185,16 +231,19 @@ __device__ __forceinline__ void issue_unit_loads(
     }
     const int vrow = vb * kBV + tid;
 #pragma unroll
-    for (int s = 0; s < TM; ++s)
-        R.vwin[s] = (U.ok && s < T && vrow < V) ? v[(((size_t)bb * T + s) * HV + hv) * V + vrow]
-                                                 : __float2bfloat16_rn(0.0f);
+    for (int s = 0; s < TM; ++s) R.vwin[s] = __float2bfloat16_rn(0.0f);
+    if (U.ok && vrow < V) {
+#pragma unroll
+        for (int s = 0; s < TM; ++s)
+            if (s < T) R.vwin[s] = v[(((size_t)bb * T + s) * HV + hv) * V + vrow];
+    }
 }
 
 // Persistent: each CTA takes units blockIdx.x, blockIdx.x + gridDim.x, ...
 // While a unit waits for its checkpoint tile and output MMA, the CTA already
 // reads the next unit's cursors and issues that unit's key/gate/value loads.
 template <int TM>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, CursorArgs C,
                  const int32_t *__restrict__ slot_idx, int nunits,
                  const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -266,6 +315,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         const size_t sh_hv = (size_t)slot * HV + hv, sh_h = (size_t)slot * H + h;
         const bool k_writer = (hv % P.G == 0) && vb == 0;
         bool waited = true;
+        int f_slot = -1, f_wp = 0, f_base = 0;   // the next unit's fetch (thread 32)
+        if (ok && tid == 32 && un < nunits) {     // fetch stage 1: the slot index
+            int bbn, hvn, vbn;
+            unit_coords(un, HV, VB, bbn, hvn, vbn);
+            f_slot = slot_idx[bbn];
+        }
 
         if (ok) {
             // ---- 1. normalise the token rows (loaded earlier) into X (SW128
@@ -392,6 +447,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             waited = ptx::mbar_wait(bar_gram, ph_gram);
             ph_gram ^= 1u;
             ptx::tc_fence_after_sync();
+            if (tid == 32 && f_slot >= 0 && f_slot < C.num_slots) {  // fetch stage 2: cursors
+                f_wp = C.write_pos[f_slot];
+                f_base = C.cache_base[f_slot];
+            }
 
             // ---- 3. per token i (thread i): row i of A (zero above the diagonal), row i of F
             {
@@ -522,8 +581,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                             make_float4(ce[s], ce[s + 1], ce[s + 2], ce[s + 3]);
                     }
                 }
-            } else if (tid == 32) {
-                fetch_unit(P, C, slot_idx, un, nunits, VB, misc);
             }
             __syncthreads();
 
@@ -613,6 +670,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             }
             if (!vh_ok && tid == 0) misc[5] = 1;
             ptx::fence_proxy_async_smem();
+            if (tid == 32)   // fetch stage 3: checks, L2 prefetch, hand-over
+                finish_fetch(P, C, un, nunits, VB, f_slot, f_wp, f_base, misc);
         }
         __syncthreads();   // next unit's cursors visible; R0 free for the checkpoint tile
 
@@ -720,14 +779,29 @@ cudaError_t launch_tm(const CUtensorMap &tmap, const LayerArgs &P, const CursorA
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
+    // all of the unified L1 / shared storage as shared memory
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    // CTAs per SM from the resources themselves: shared memory (with the
+    // per-CTA reserve) and kCtasPerSm.  The runtime's occupancy query answers 1
+    // for this kernel whatever the sizes, yet the SM holds three of its CTAs
+    // (measured: all 3 x SMs CTAs of one launch start within a few
+    // microseconds), and one per SM would leave two thirds of the machine idle.
+    int dev = 0, sms = 0, smem_sm = 0, smem_rsv = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, tc::kThreads,
-                                                           tc::kSmemBytes)) != cudaSuccess)
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+        cudaSuccess)
         return e;
+    if ((e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+        cudaSuccess)
+        return e;
+    int per_sm = smem_sm / (tc::kSmemBytes + smem_rsv);
+    if (per_sm > tc::kCtasPerSm) per_sm = tc::kCtasPerSm;
+    if (per_sm < 1) per_sm = 1;
     const int nunits = B * P.HV * (P.V / tc::kBV);
-    int grid = sms * (per_sm > 0 ? per_sm : 1);
+    int grid = sms * per_sm;
     if (grid > nunits) grid = nunits;
     kern<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(
         tmap, P, C, slot_idx, nunits, static_cast<const __nv_bfloat16 *>(q),
