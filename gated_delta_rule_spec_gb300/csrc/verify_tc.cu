@@ -184,9 +184,14 @@ __device__ __forceinline__ void fetch_unit(const LayerArgs &P, const CursorArgs 
 template <int TM>
 struct UnitLoads {
     uint4 raw[8];
-    float g_in, b_in, alog, dtb;
-    __nv_bfloat16 vwin[TM];
+    // raw 32-bit words, converted only when the unit uses them: the ring's
+    // fp32 gates, or the window's bf16 gate inputs and values zero-extended
+    uint32_t g_in, b_in;
+    float alog, dtb;
+    uint32_t vwin[TM];
 };
+
+__device__ __forceinline__ float bf16_word_to_float(uint32_t w) { return __uint_as_float(w << 16); }
 
 template <int TM>
 __device__ __forceinline__ void issue_unit_loads(
@@ -217,25 +222,27 @@ __device__ __forceinline__ void issue_unit_loads(
 #pragma unroll
         for (int c = 0; c < 8; ++c) R.raw[c] = s4[c];
     }
-    R.g_in = R.b_in = R.alog = R.dtb = 0.0f;
+    R.g_in = R.b_in = 0u;
+    R.alog = R.dtb = 0.0f;
     if (U.ok && tid < W) {
         const int pj = ring_pos(base, tid, L);
-        R.g_in = P.ring_g[sh_hv * L + pj];
-        R.b_in = P.ring_beta[sh_hv * L + pj];
+        R.g_in = reinterpret_cast<const uint32_t *>(P.ring_g)[sh_hv * L + pj];
+        R.b_in = reinterpret_cast<const uint32_t *>(P.ring_beta)[sh_hv * L + pj];
     } else if (U.ok && tid < n) {
         const size_t tok = (size_t)bb * T + (tid - W);
-        R.g_in = __bfloat162float(a[tok * HV + hv]);
-        R.b_in = __bfloat162float(bgate[tok * HV + hv]);
+        R.g_in = reinterpret_cast<const unsigned short *>(a)[tok * HV + hv];
+        R.b_in = reinterpret_cast<const unsigned short *>(bgate)[tok * HV + hv];
         R.alog = A_log[hv];
         R.dtb = dt_bias[hv];
     }
     const int vrow = vb * kBV + tid;
 #pragma unroll
-    for (int s = 0; s < TM; ++s) R.vwin[s] = __float2bfloat16_rn(0.0f);
+    for (int s = 0; s < TM; ++s) R.vwin[s] = 0u;
     if (U.ok && vrow < V) {
 #pragma unroll
         for (int s = 0; s < TM; ++s)
-            if (s < T) R.vwin[s] = v[(((size_t)bb * T + s) * HV + hv) * V + vrow];
+            if (s < T)
+                R.vwin[s] = reinterpret_cast<const unsigned short *>(v)[(((size_t)bb * T + s) * HV + hv) * V + vrow];
     }
 }
 
@@ -384,10 +391,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             }
             if (tid < n) {
                 const int pj = ring_pos(base, tid, L);
-                float g = R.g_in, be = R.b_in;
+                float g = __uint_as_float(R.g_in), be = __uint_as_float(R.b_in);
                 if (tid >= W) {
-                    g = gate_g(R.alog, R.g_in, R.dtb);
-                    be = gate_beta(R.b_in);
+                    g = gate_g(R.alog, bf16_word_to_float(R.g_in), R.dtb);
+                    be = gate_beta(bf16_word_to_float(R.b_in));
                     if (vb == 0) {
                         P.ring_g[sh_hv * L + pj] = g;
                         P.ring_beta[sh_hv * L + pj] = be;
@@ -398,7 +405,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             }
 #pragma unroll
             for (int s = 0; s < TM; ++s)
-                if (s < T && vrow < V) rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = R.vwin[s];
+                if (s < T && vrow < V) rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] =
+                        __ushort_as_bfloat16((unsigned short)R.vwin[s]);
             ptx::fence_proxy_async_smem();
             __syncthreads();
 
@@ -656,7 +664,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
 #pragma unroll
                 for (int s2 = 0; s2 < TM; ++s2) {
                     if (s2 < T) {
-                        const float x = __bfloat162float(R.vwin[s2]);
+                        const float x = bf16_word_to_float(R.vwin[s2]);
 #pragma unroll
                         for (int s = 0; s < TM; s += 4) {
                             const float4 c4 = *reinterpret_cast<const float4 *>(sm + c_off(W + s2) + 4 * s);
