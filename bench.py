@@ -15,7 +15,8 @@ which are not available here).
 A step is one decode round of the layer: verify (output of the whole draft
 window, ring side channel) -> commit(accept_len) -> fold (exact, only slots whose
 is_flush is set; cursors move after).  Steps are captured in CUDA graphs and
-timed with CUDA events; timing events inside the graph bracket every verify, so
+timed with CUDA events; timing events inside the graph bracket every tenth
+verify (an event node between kernels costs the step a few microseconds), so
 the verify kernel's own duration is measured in the timed region.  The
 checkpoint working set (B x 32 x 64 KiB = 256 MiB at B=128) exceeds L2.
 
@@ -234,19 +235,24 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     inputs = [dev_window() for _ in range(NI)]
     acc_np = np.stack([gen.accept_lens(rng, wl.B, wl.T) for _ in range(R)])
     acc_dev = torch.from_numpy(acc_np).to(device)
+    # events bracket every EV_EVERY-th verify of the timed graph: an event node
+    # between kernels costs the step several microseconds, so sample
+    EV_EVERY = 10 if R >= 20 else 1
+    ev_steps = list(range(0, R, EV_EVERY))
     try:
-        ev = [(torch.cuda.Event(enable_timing=True, external=True),
-               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(R)]
+        ev = {i: (torch.cuda.Event(enable_timing=True, external=True),
+                  torch.cuda.Event(enable_timing=True, external=True)) for i in ev_steps}
     except TypeError:  # torch without external events: time verify in its own graph below
         ev = None
 
     def step(i, timed_events=True):
         w = inputs[i % NI]
-        if timed_events and ev is not None:
+        timed = timed_events and ev is not None and i in ev
+        if timed:
             ev[i][0].record()
         binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias,
                        out=outs[i % NI])
-        if timed_events and ev is not None:
+        if timed:
             ev[i][1].record()
         binding.commit(cur, wl.T, wl.L, slots, acc_dev[i % R])
         binding.fold(layer, cur, slots)
@@ -295,7 +301,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     verify_ms = []
     if args.steps // R > 0 and ev is not None:
         try:
-            verify_ms = [a.elapsed_time(b) for a, b in ev]
+            verify_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in ev_steps]
         except RuntimeError:
             verify_ms = []
     if not verify_ms:
@@ -313,6 +319,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     W_all = mirror_cursors(wp0, None, acc_seq[args.warmup:], wl.T, wl.L)
     last = slice((args.steps // R - 1) * R, (args.steps // R) * R)
     W_last = W_all[last] if args.steps // R > 0 else W_all
+    if args.steps // R > 0 and ev is not None:   # the verifies the events bracketed
+        W_last = W_last[ev_steps]
     bytes_per_launch = float(np.mean([
         verify_bytes_per_unit(Wr, wl.K, wl.V, wl.T, wl.G, wl.e, False).sum() * wl.HV
         for Wr in W_last]))

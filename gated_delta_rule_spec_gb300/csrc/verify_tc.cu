@@ -685,8 +685,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
 
         // ---- 6. checkpoint tile by TMA (over the dead key buffers); the next
         //         unit's loads go out while it is in flight; then P = S0 q_eff^T
+        // (every thread fenced its generic shared-memory accesses before the
+        // barrier above: no further proxy fence is needed before the TMA)
         if (ok && tid == 0) {
-            ptx::fence_proxy_async_smem();
             ptx::mbar_expect_tx(bar_s0, kR0Bytes);
             const int32_t y = (int32_t)((sh_hv * V) + v0);
 #pragma unroll

@@ -107,6 +107,20 @@ def test_c2_batch_sweep_scattered_slots(B):
     sc.check_ring()
 
 
+def test_repeated_verify_same_bits_several_units_per_cta():
+    """B = 256 rows x 32 v-heads is several units per persistent CTA; each unit
+    is computed by one CTA alone, so repeated verifies of the same window give
+    the same bits."""
+    wl = WL["C2"]
+    sc = Scenario(wl, B=256, seed=11, num_slots=512, random_cursors=True)
+    w = sc.window()
+    out1, _, _ = sc.verify(w, run_oracle=False)
+    out1 = out1.clone()
+    for _ in range(3):
+        out2, _, _ = sc.verify(w, run_oracle=False)
+        assert torch.equal(out1, out2)
+
+
 def test_output_independent_of_window_ring_contents_and_repeatable():
     """The ring write is a side channel: the output does not depend on what the
     window's ring positions held before, and a repeated verify (which rewrites
