@@ -22,7 +22,7 @@ cudaError_t launch_verify_tc(const LayerArgs &P, const CursorArgs &C, const int3
 cudaError_t launch_fold(const LayerArgs &P, const FoldLayers &FL, int n_layers, bool kda,
                         bool bf16, const CursorArgs &C, const int32_t *slot_idx, int B,
                         cudaStream_t stream);
-size_t fold_smem_bytes(int K, int L, bool kda);
+size_t fold_smem_bytes(int K, int L, bool kda, bool bf16);
 cudaError_t launch_commit(const CursorArgs &C, int T, int L, const int32_t *slot_idx, int B,
                           const int32_t *accept_len, cudaStream_t stream);
 cudaError_t launch_fold_cursors(const CursorArgs &C, int L, const int32_t *slot_idx, int B,
@@ -176,7 +176,7 @@ int gdn_spec_fold(const gdn_spec_layer *layers, int32_t n_layers, const gdn_spec
     if (!slot_idx) return GDN_SPEC_EINVAL;
     const bool kda = layers[0].gate_kind == GDN_SPEC_GATE_PER_KEY;
     const bool bf16 = layers[0].io_dtype == GDN_SPEC_DTYPE_BF16;
-    if (fold_smem_bytes(layers[0].K, layers[0].L, kda) > kMaxSmem) return GDN_SPEC_EUNSUPPORTED;
+    if (fold_smem_bytes(layers[0].K, layers[0].L, kda, bf16) > kMaxSmem) return GDN_SPEC_EUNSUPPORTED;
     const LayerArgs P = layer_args(&layers[0]);
     const CursorArgs C = cursor_args(cursors);
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -7,64 +7,134 @@
 // item 3).  This kernel does exactly that, in fp32, token by token:
 //     S <- exp(g_t) S   (KDA: S diag(exp(g_t)))
 //     d  = beta_t (v_t - S k^_t),   S <- S + d k^_t^T
-// Rows of S are independent under the recurrence (row i only sees v_t[i]),
-// so four threads own one state row (K/4 values each, in registers; the row's
-// dot product takes two shuffles) and replay the records one after another.
-// The elementwise work uses Blackwell's packed fp32x2 instructions.
+//
+// Rows of S are independent under the recurrence (row i only sees v_t[i]).
+// A thread owns one quarter of the K columns of TWO state rows (rows p and
+// p + 32 of a 64-row block; a row's dot product takes two shuffles), so
+// every key value it reads from shared memory serves both rows.  The keys
+// stay in shared memory as the raw I/O-dtype records (bf16: half the bytes
+// of fp32) and are widened in registers: reading the keys is what bounds the
+// replay, and the two choices together cut that traffic per state row by
+// four.  The elementwise work uses Blackwell's packed fp32x2 instructions.
+//
+// With one gate per (token, v-head) the decay is carried as a running scalar
+// instead of being applied to every element: S = gam * R with gam the product
+// of the decays so far, so a record costs a dot product and a rank-1 update of
+// R and nothing else:
+//     gam <- gam * exp(g_t),  u = R k^_t,  R <- R + beta_t (v_t / gam - u) k^_t^T
+// (since exp(g_t) S_{t-1} = gam_t R_{t-1}).  When gam drops below 2^-32 it is
+// multiplied into R and reset to 1, which keeps every value in range; the
+// stored checkpoint is gam * R.  This is the same recurrence, record by
+// record, with the decay multiplications moved, not a chunked form.
 //
 // Only the rows whose is_flush is set do any work, and in steady state that
 // is a small share of the batch per step.  So the grid is persistent: every
-// CTA scans the batch's flags, builds the same compact list of rows to fold,
-// and takes work items (row, layer, v-head, block of 32 state rows)
-// round-robin from it.  For an item every global read (keys, gates, values,
-// the state rows) is issued in one round.  Folding runs after sampling,
-// outside the forward, so the layers are independent here and one launch
-// folds all of them (the blog's §2.1 observation about replay outside the
-// forward).  The cursors move in a separate launch after every layer.
+// CTA scans the batch's flags, builds the same compact list of slots to
+// fold, and takes work items (row, layer, v-head, block of 64 state rows)
+// round-robin from it.  An item's keys (one or two contiguous ring segments)
+// and values (one short run per record) arrive by bulk asynchronous copies
+// on an mbarrier while the CTA reads the gates and loads its state rows into
+// registers.  Folding runs after sampling, outside the forward, so the
+// layers are independent here and one launch folds all of them (the blog's
+// §2.1 observation about replay outside the forward).  The cursors move in
+// a separate launch after every layer.
 #include "common.cuh"
+#include "ptx_sm100.cuh"
 
 namespace gdnspec {
 
 constexpr int kFoldThreads = 128;
-constexpr int kFoldTPR = 4;                          // threads per state row
-constexpr int kFoldRows = kFoldThreads / kFoldTPR;   // state rows per work item
-constexpr int kFoldMaxL = 128;   // ring length limit of this kernel
+constexpr int kFoldTPR = 4;                           // threads per pair of state rows
+constexpr int kFoldPairs = kFoldThreads / kFoldTPR;   // 32
+constexpr int kFoldRows = 2 * kFoldPairs;             // state rows per work item
+constexpr int kFoldMaxL = 128;                        // ring length limit of this kernel
 constexpr int kFoldScan = kFoldThreads;
 
-// Shared memory of one item: raw keys [L][K] fp32, alpha [L] (KDA [L][K]),
-// beta [L], 1/|k| [L], values [L][32 rows] fp32, and the compacted row list.
-size_t fold_smem_bytes(int K, int L, bool kda) {
-    return sizeof(float) * ((size_t)L * K + (size_t)L * (kda ? K : 1) + 2 * L + (size_t)L * kFoldRows) +
-           sizeof(int) * 2 * kFoldScan;
+__host__ __device__ constexpr size_t fold_pad16(size_t bytes) { return (bytes + 15) & ~(size_t)15; }
+
+// Shared memory of one item (every region starts on 16 bytes): raw keys
+// [L][K] and raw values [L][64 rows] in the I/O dtype, then fp32 (alpha,
+// 1/alpha) [L] (KDA: alpha [L][K]), beta [L], 1/|k| [L], and the compacted
+// slot list with its cursors.
+struct FoldSmem {
+    size_t keys, vals, alpha, beta, rs, rows, meta, total;
+    __host__ __device__ FoldSmem(int K, int L, bool kda, size_t io) {
+        keys = 0;
+        vals = keys + fold_pad16((size_t)L * K * io);
+        alpha = vals + fold_pad16((size_t)L * kFoldRows * io);
+        beta = alpha + fold_pad16(sizeof(float) * (size_t)L * (kda ? K : 2));
+        rs = beta + fold_pad16(sizeof(float) * L);
+        rows = rs + fold_pad16(sizeof(float) * L);
+        meta = rows + sizeof(int) * kFoldScan;
+        total = meta + sizeof(int) * kFoldScan;
+    }
+};
+
+size_t fold_smem_bytes(int K, int L, bool kda, bool bf16) {
+    return FoldSmem(K, L, kda, bf16 ? 2 : 4).total;
 }
+
+// 16 bytes of raw keys -> fp32 pairs (bf16: 8 values, fp32: 4)
+template <typename IO> struct KeyChunk;
+template <> struct KeyChunk<__nv_bfloat16> {
+    static constexpr int kVals = 8;
+    __device__ __forceinline__ static void widen(const uint4 &w, float2 (&x)[4]) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)   // the low half is the element at the lower address
+            x[i] = make_float2(__uint_as_float(q[i] << 16), __uint_as_float(q[i] & 0xFFFF0000u));
+    }
+};
+template <> struct KeyChunk<float> {
+    static constexpr int kVals = 4;
+    __device__ __forceinline__ static void widen(const uint4 &w, float2 (&x)[2]) {
+        x[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+        x[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+    }
+};
 
 template <typename IO, bool KDA, int K>
 __global__ void __launch_bounds__(kFoldThreads, 4)
 fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int32_t *__restrict__ slot_idx, int B) {
-    static_assert(K % 32 == 0 && K <= 128, "K/4 state values per thread, in float4 chunks");
-    constexpr int KC = K / 16;   // float4 chunks per thread: chunk c4 = part + 4 m
-    extern __shared__ __align__(16) float sm[];
+    static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
+    using KC = KeyChunk<IO>;
+    constexpr int kPer = KC::kVals;                 // key values per 16-byte chunk
+    constexpr int kNC = K / kPer / kFoldTPR;        // chunks per thread: chunk part + 4 m
+    constexpr int kNP = kNC * kPer / 2;             // float2 pairs per thread and row
+    static_assert(kNC >= 1, "at least one chunk per thread");
+    extern __shared__ __align__(16) uint8_t smem[];
     __shared__ int s_count, s_warp_off[kFoldThreads / 32];
+    __shared__ __align__(8) uint64_t s_bar;
     const int V = P.V, L = P.L, HV = P.HV, H = P.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float *Xs = sm;                                  // [L][K]
-    float *alpha = Xs + (size_t)L * K;               // [L] or [L][K]
-    float *betaS = alpha + (size_t)L * (KDA ? K : 1);
-    float *rsS = betaS + L;                          // [L] 1 / |k_t|
-    float *vv = rsS + L;                             // [L][kFoldRows]
-    int *rows = reinterpret_cast<int *>(vv + (size_t)L * kFoldRows);
-    int *meta = rows + kFoldScan;
+    const FoldSmem lay(K, L, KDA, sizeof(IO));
+    IO *Xk = reinterpret_cast<IO *>(smem + lay.keys);      // [L][K]
+    IO *Xv = reinterpret_cast<IO *>(smem + lay.vals);      // [L][kFoldRows]
+    float *alpha = reinterpret_cast<float *>(smem + lay.alpha);
+    float *betaS = reinterpret_cast<float *>(smem + lay.beta);
+    float *rsS = reinterpret_cast<float *>(smem + lay.rs);
+    int *rows = reinterpret_cast<int *>(smem + lay.rows);
+    int *meta = reinterpret_cast<int *>(smem + lay.meta);
+    const uint32_t bar = ptx::smem_addr(&s_bar);
     const int vblocks = (V + kFoldRows - 1) / kFoldRows;
     const int per_row = n_layers * HV * vblocks;
+    const int pair = tid / kFoldTPR, part = tid % kFoldTPR;
     long long item_base = 0;  // items enumerated in earlier scan passes
+    uint32_t phase = 0;
+
+    if (tid == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::mbar_init_fence();
+    }
+    __syncthreads();
 
     for (int b0 = 0; b0 < B; b0 += kFoldScan) {
         // ---- scan kFoldScan batch rows, compact the flagged ones (same list in every CTA)
         const int bb = b0 + tid;
-        int flag = 0, wp = 0, base = 0;
+        int flag = 0, wp = 0, base = 0, slot = -1;
         if (bb < B) {
-            const int slot = slot_idx[bb];
+            slot = slot_idx[bb];
             if (slot >= 0 && slot < C.num_slots && C.is_flush[slot]) {
                 wp = C.write_pos[slot];
                 base = C.cache_base[slot];
@@ -86,7 +156,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
         __syncthreads();
         if (flag) {
             const int pos = s_warp_off[warp] + __popc(ball & ((1u << lane) - 1u));
-            rows[pos] = bb;
+            rows[pos] = slot;
             meta[pos] = (wp << 16) | base;
         }
         __syncthreads();
@@ -102,167 +172,192 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             rem -= li * HV * vblocks;
             const int hv = rem / vblocks, vbk = rem - hv * vblocks;
             const int h = hv / P.G;
-            const int slot = slot_idx[rows[e]];
-            const int W = meta[e] >> 16, base = meta[e] & 0xFFFF;
-            const int r = tid / kFoldTPR, part = tid % kFoldTPR;
-            const int vr = vbk * kFoldRows + r;   // this thread's state row
-            const bool valid = vr < V;
-            const size_t sh_hv = (size_t)slot * HV + hv, sh_h = (size_t)slot * H + h;
+            const int slot_e = rows[e];
+            const int W = meta[e] >> 16, base_e = meta[e] & 0xFFFF;
+            const int row0 = vbk * kFoldRows;
+            const int nrows = V - row0 < kFoldRows ? V - row0 : kFoldRows;   // a multiple of 8
+            const size_t sh_hv = (size_t)slot_e * HV + hv, sh_h = (size_t)slot_e * H + h;
             const IO *rawk = reinterpret_cast<const IO *>(FL.rawk[li]);
             const IO *rawv = reinterpret_cast<const IO *>(FL.rawv[li]);
             const float *ring_g = FL.ring_g[li];
             const float *ring_beta = FL.ring_beta[li];
             float *ckpt = FL.checkpoint[li];
 
-            // ---- one round of reads: the state row slice, keys (two threads per
-            //      record), gates (thread per record), values
-            float2 S2[2 * KC];
-            const float4 *srow = reinterpret_cast<const float4 *>(ckpt + (sh_hv * V + (valid ? vr : 0)) * K);
-#pragma unroll
-            for (int m = 0; m < KC; ++m) {
-                const float4 t4 = valid ? srow[part + 4 * m] : make_float4(0.f, 0.f, 0.f, 0.f);
-                S2[2 * m] = make_float2(t4.x, t4.y);
-                S2[2 * m + 1] = make_float2(t4.z, t4.w);
-            }
-            // keys stay raw in shared memory; rs[t] = 1 / |k_t| (with eps) is
-            // applied in the replay.  All loads of the item are issued before
-            // any of them is used: keys of records tid/2 (+64 per pass), the
-            // gates of record tid, the values of this thread's records.
-            constexpr int KH = K / 2;                    // key elements per thread
-            constexpr int kPer = 16 / (int)sizeof(IO);
-            constexpr int kChunks = KH / kPer;
-            const int half = tid & 1;
-            uint4 kraw[kChunks];
-            {
-                const int j = tid >> 1;
-                if (j < W) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        rawk + (sh_h * L + ring_pos(base, j, L)) * K + half * KH);
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) kraw[c] = src[c];
+            // ---- 1. keys and values by bulk copies (warp 0): the keys are one
+            //         or two contiguous ring segments, the values one run of
+            //         nrows per record
+            if (warp == 0) {
+                const uint32_t kbytes = (uint32_t)(K * sizeof(IO)), vbytes = (uint32_t)(nrows * sizeof(IO));
+                if (lane == 0) {
+                    ptx::fence_proxy_async_smem();   // the previous item's generic reads come first
+                    ptx::mbar_expect_tx(bar, (uint32_t)W * (kbytes + vbytes));
+                    const int n1 = (L - base_e) < W ? (L - base_e) : W;
+                    ptx::bulk_copy_g2s(ptx::smem_addr(Xk), rawk + (sh_h * L + base_e) * K, n1 * kbytes, bar);
+                    if (W > n1)
+                        ptx::bulk_copy_g2s(ptx::smem_addr(Xk + (size_t)n1 * K), rawk + sh_h * L * K,
+                                           (W - n1) * kbytes, bar);
                 }
+                __syncwarp();
+                for (int j = lane; j < W; j += 32)
+                    ptx::bulk_copy_g2s(ptx::smem_addr(Xv + (size_t)j * kFoldRows),
+                                       rawv + (sh_hv * L + ring_pos(base_e, j, L)) * V + row0, vbytes, bar);
             }
-            float g_in = 0.f, b_in = 0.f;
-            if (tid < W) {
-                const int p = ring_pos(base, tid, L);
-                if (!KDA) g_in = ring_g[sh_hv * L + p];
-                b_in = ring_beta[sh_hv * L + p];
-            }
-            float xv[kFoldMaxL / kFoldTPR];
-#pragma unroll
-            for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
-                const int j = part + kFoldTPR * u;
-                xv[u] = (j < W && valid) ? to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vr])
-                                         : 0.0f;
-            }
-            // keys -> shared memory (first 64 records from the registers above)
-            for (int pass = 0; pass * (kFoldThreads / 2) < W; ++pass) {
-                const int j = pass * (kFoldThreads / 2) + (tid >> 1);
-                if (pass > 0 && j < W) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(
-                        rawk + (sh_h * L + ring_pos(base, j, L)) * K + half * KH);
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) kraw[c] = src[c];
+            // ---- 2. gates (thread per record) and this thread's two state rows
+            for (int j = tid; j < W; j += kFoldThreads) {
+                const int p = ring_pos(base_e, j, L);
+                if (!KDA) {
+                    const float gj = ring_g[sh_hv * L + p];
+                    reinterpret_cast<float2 *>(alpha)[j] = make_float2(expf(gj), expf(-gj));
                 }
-                float ss = 0.0f;
-                if (j < W) {
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        float x[kPer];
-                        const uint4 u4 = kraw[c];
-                        if constexpr (sizeof(IO) == 2) {
-                            const uint32_t w[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-                                x[2 * e] = f.x;
-                                x[2 * e + 1] = f.y;
-                            }
-                        } else {
-                            x[0] = __uint_as_float(u4.x); x[1] = __uint_as_float(u4.y);
-                            x[2] = __uint_as_float(u4.z); x[3] = __uint_as_float(u4.w);
-                        }
-#pragma unroll
-                        for (int e = 0; e < kPer; e += 4) {
-                            ss = fmaf(x[e], x[e], ss); ss = fmaf(x[e + 1], x[e + 1], ss);
-                            ss = fmaf(x[e + 2], x[e + 2], ss); ss = fmaf(x[e + 3], x[e + 3], ss);
-                            *reinterpret_cast<float4 *>(Xs + j * K + half * KH + c * kPer + e) =
-                                make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-                        }
-                    }
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                if (j < W && half == 0) rsS[j] = 1.0f / sqrtf(ss + P.l2_eps);
+                betaS[j] = ring_beta[sh_hv * L + p];
             }
             if (KDA) {
                 for (int idx = tid; idx < W * K; idx += kFoldThreads) {
                     const int j = idx / K, kk = idx - j * K;
-                    alpha[idx] = expf(ring_g[(sh_hv * L + ring_pos(base, j, L)) * K + kk]);
+                    alpha[idx] = expf(ring_g[(sh_hv * L + ring_pos(base_e, j, L)) * K + kk]);
                 }
-            } else if (tid < W) {
-                alpha[tid] = expf(g_in);
             }
-            if (tid < W) betaS[tid] = b_in;
-            for (int j = kFoldThreads + tid; j < W; j += kFoldThreads) {  // records >= 128 (none: L <= 128)
-                if (!KDA) alpha[j] = expf(ring_g[sh_hv * L + ring_pos(base, j, L)]);
-                betaS[j] = ring_beta[sh_hv * L + ring_pos(base, j, L)];
-            }
+            float2 S[2][kNP];
+            const bool valid0 = pair < nrows, valid1 = pair + kFoldPairs < nrows;
 #pragma unroll
-            for (int u = 0; u < kFoldMaxL / kFoldTPR; ++u) {
-                const int j = part + kFoldTPR * u;
-                if (j < W) vv[j * kFoldRows + r] = xv[u];
+            for (int rr = 0; rr < 2; ++rr) {
+#pragma unroll
+                for (int i = 0; i < kNP; ++i) S[rr][i] = make_float2(0.f, 0.f);
+                if (rr ? valid1 : valid0) {
+                    const float *srow = ckpt + (sh_hv * V + row0 + pair + rr * kFoldPairs) * K;
+#pragma unroll
+                    for (int m = 0; m < kNC; ++m) {
+                        const float4 *src = reinterpret_cast<const float4 *>(srow + (part + 4 * m) * kPer);
+#pragma unroll
+                        for (int q = 0; q < kPer / 4; ++q) {
+                            const float4 f = src[q];
+                            S[rr][m * (kPer / 2) + 2 * q] = make_float2(f.x, f.y);
+                            S[rr][m * (kPer / 2) + 2 * q + 1] = make_float2(f.z, f.w);
+                        }
+                    }
+                }
+            }
+            // ---- 3. the copies land; 1 / |k_t| for every record (two threads each)
+            const bool landed = ptx::mbar_wait(bar, phase);
+            phase ^= 1u;
+            if (__syncthreads_or(!landed)) {   // the same decision in every thread
+                // record the failure, give the copies one more bounded wait so
+                // that none is still writing this CTA's shared memory, and stop
+                if (tid == 0) atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
+                ptx::mbar_wait(bar, phase ^ 1u);
+                return;
+            }
+            // (the trip count is the same in every thread: the shuffle is warp-wide)
+            for (int j0 = 0; j0 < W; j0 += kFoldThreads / 2) {
+                const int j = j0 + (tid >> 1);
+                float ss = 0.0f;
+                if (j < W) {
+                    const uint4 *kr =
+                        reinterpret_cast<const uint4 *>(Xk + (size_t)j * K) + (tid & 1) * (K / kPer / 2);
+#pragma unroll
+                    for (int c = 0; c < K / kPer / 2; ++c) {
+                        float2 x[kPer / 2];
+                        KC::widen(kr[c], x);
+#pragma unroll
+                        for (int i = 0; i < kPer / 2; ++i) ss = fmaf(x[i].y, x[i].y, fmaf(x[i].x, x[i].x, ss));
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (j < W && (tid & 1) == 0) rsS[j] = 1.0f / sqrtf(ss + P.l2_eps);
             }
             __syncthreads();
 
-            // ---- replay (decay, then the delta against the decayed state)
+            // ---- 4. replay (decay, then the delta against the decayed state)
+            float gam = 1.0f, inv = 1.0f;   // scalar gate: S = gam R (every thread holds the same values)
             for (int t = 0; t < W; ++t) {
-                const float4 *xk = reinterpret_cast<const float4 *>(Xs + t * K);
-                float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                if (KDA) {
-                    const float4 *al = reinterpret_cast<const float4 *>(alpha + (size_t)t * K);
+                const uint4 *xk = reinterpret_cast<const uint4 *>(Xk + (size_t)t * K);
+                float2 x[kNP];
 #pragma unroll
-                    for (int m = 0; m < KC; ++m) {
-                        const float4 a4 = al[part + 4 * m], x4 = xk[part + 4 * m];
-                        S2[2 * m] = __fmul2_rn(S2[2 * m], make_float2(a4.x, a4.y));
-                        S2[2 * m + 1] = __fmul2_rn(S2[2 * m + 1], make_float2(a4.z, a4.w));
-                        acc[0] = __ffma2_rn(S2[2 * m], make_float2(x4.x, x4.y), acc[0]);
-                        acc[1] = __ffma2_rn(S2[2 * m + 1], make_float2(x4.z, x4.w), acc[1]);
+                for (int m = 0; m < kNC; ++m) {
+                    float2 c2[kPer / 2];
+                    KC::widen(xk[part + 4 * m], c2);
+#pragma unroll
+                    for (int i = 0; i < kPer / 2; ++i) x[m * (kPer / 2) + i] = c2[i];
+                }
+                if (KDA) {
+                    const float *al = alpha + (size_t)t * K;
+#pragma unroll
+                    for (int m = 0; m < kNC; ++m) {
+                        const float4 *a4 = reinterpret_cast<const float4 *>(al + (part + 4 * m) * kPer);
+#pragma unroll
+                        for (int q = 0; q < kPer / 4; ++q) {
+                            const float4 a = a4[q];
+                            const int i = m * (kPer / 2) + 2 * q;
+#pragma unroll
+                            for (int rr = 0; rr < 2; ++rr) {
+                                S[rr][i] = __fmul2_rn(S[rr][i], make_float2(a.x, a.y));
+                                S[rr][i + 1] = __fmul2_rn(S[rr][i + 1], make_float2(a.z, a.w));
+                            }
+                        }
                     }
                 } else {
-                    const float a = alpha[t];
-                    const float2 a2 = make_float2(a, a);
+                    const float2 ai = reinterpret_cast<const float2 *>(alpha)[t];   // (alpha, 1 / alpha)
+                    gam *= ai.x;
+                    inv *= ai.y;
+                    if (gam < 0x1p-32f) {   // the same branch in every thread
+                        const float2 g2 = make_float2(gam, gam);
 #pragma unroll
-                    for (int m = 0; m < KC; ++m) {
-                        const float4 x4 = xk[part + 4 * m];
-                        S2[2 * m] = __fmul2_rn(S2[2 * m], a2);
-                        S2[2 * m + 1] = __fmul2_rn(S2[2 * m + 1], a2);
-                        acc[0] = __ffma2_rn(S2[2 * m], make_float2(x4.x, x4.y), acc[0]);
-                        acc[1] = __ffma2_rn(S2[2 * m + 1], make_float2(x4.z, x4.w), acc[1]);
+                        for (int i = 0; i < kNP; ++i) {
+                            S[0][i] = __fmul2_rn(S[0][i], g2);
+                            S[1][i] = __fmul2_rn(S[1][i], g2);
+                        }
+                        gam = 1.0f;
+                        inv = 1.0f;
                     }
                 }
-                float u = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-                u += __shfl_xor_sync(0xffffffffu, u, 1);
-                u += __shfl_xor_sync(0xffffffffu, u, 2);
-                const float rs = rsS[t];
-                const float d = betaS[t] * (vv[t * kFoldRows + r] - rs * u) * rs;
-                const float2 d2 = make_float2(d, d);
+                float2 acc[2][2] = {{make_float2(0.f, 0.f), make_float2(0.f, 0.f)},
+                                    {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}};
 #pragma unroll
-                for (int m = 0; m < KC; ++m) {
-                    const float4 x4 = xk[part + 4 * m];
-                    S2[2 * m] = __ffma2_rn(d2, make_float2(x4.x, x4.y), S2[2 * m]);
-                    S2[2 * m + 1] = __ffma2_rn(d2, make_float2(x4.z, x4.w), S2[2 * m + 1]);
+                for (int i = 0; i < kNP; ++i) {
+                    acc[0][i & 1] = __ffma2_rn(S[0][i], x[i], acc[0][i & 1]);
+                    acc[1][i & 1] = __ffma2_rn(S[1][i], x[i], acc[1][i & 1]);
+                }
+                float u0 = (acc[0][0].x + acc[0][0].y) + (acc[0][1].x + acc[0][1].y);
+                float u1 = (acc[1][0].x + acc[1][0].y) + (acc[1][1].x + acc[1][1].y);
+                u0 += __shfl_xor_sync(0xffffffffu, u0, 1);
+                u1 += __shfl_xor_sync(0xffffffffu, u1, 1);
+                u0 += __shfl_xor_sync(0xffffffffu, u0, 2);
+                u1 += __shfl_xor_sync(0xffffffffu, u1, 2);
+                const float rs = rsS[t], be = betaS[t];
+                const float v0 = to_f32<IO>(Xv[(size_t)t * kFoldRows + pair]);
+                const float v1 = to_f32<IO>(Xv[(size_t)t * kFoldRows + pair + kFoldPairs]);
+                // KDA: S itself (inv stays 1); scalar gate: R, with v_t / gam
+                const float d0 = be * (v0 * inv - rs * u0) * rs;
+                const float d1 = be * (v1 * inv - rs * u1) * rs;
+                const float2 d20 = make_float2(d0, d0), d21 = make_float2(d1, d1);
+#pragma unroll
+                for (int i = 0; i < kNP; ++i) {
+                    S[0][i] = __ffma2_rn(d20, x[i], S[0][i]);
+                    S[1][i] = __ffma2_rn(d21, x[i], S[1][i]);
                 }
             }
-            if (valid) {
-                float4 *dst = reinterpret_cast<float4 *>(ckpt + (sh_hv * V + vr) * K);
+            // ---- 5. S = gam R back into the checkpoint
+            const float2 g2 = make_float2(gam, gam);
 #pragma unroll
-                for (int m = 0; m < KC; ++m)
-                    dst[part + 4 * m] = make_float4(S2[2 * m].x, S2[2 * m].y, S2[2 * m + 1].x, S2[2 * m + 1].y);
+            for (int rr = 0; rr < 2; ++rr) {
+                if (!(rr ? valid1 : valid0)) continue;
+                float *drow = ckpt + (sh_hv * V + row0 + pair + rr * kFoldPairs) * K;
+#pragma unroll
+                for (int m = 0; m < kNC; ++m) {
+                    float4 *dst = reinterpret_cast<float4 *>(drow + (part + 4 * m) * kPer);
+#pragma unroll
+                    for (int q = 0; q < kPer / 4; ++q) {
+                        const int i = m * (kPer / 2) + 2 * q;
+                        const float2 a = KDA ? S[rr][i] : __fmul2_rn(S[rr][i], g2);
+                        const float2 b = KDA ? S[rr][i + 1] : __fmul2_rn(S[rr][i + 1], g2);
+                        dst[q] = make_float4(a.x, a.y, b.x, b.y);
+                    }
+                }
             }
             __syncthreads();  // the item's buffers are reused by the next item
         }
         item_base += nitems;
-        __syncthreads();  // the row list is rebuilt by the next pass
+        __syncthreads();  // the slot list is rebuilt by the next pass
     }
 }
 
@@ -270,7 +365,7 @@ template <typename IO, bool KDA, int K>
 static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n_layers,
                                  const CursorArgs &C, const int32_t *slot_idx, int B,
                                  cudaStream_t stream) {
-    const size_t smem = fold_smem_bytes(K, P.L, KDA);
+    const size_t smem = FoldSmem(K, P.L, KDA, sizeof(IO)).total;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

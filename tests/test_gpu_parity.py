@@ -50,8 +50,11 @@ def test_c0_tiny_fp32_six_rounds(record_property):
     print(f"C0 fp32: max-abs output error {worst['out']:.3e}, checkpoint rel-Fro {worst['ckpt']:.3e}")
 
 
-@pytest.mark.parametrize("decay_shift", [0.0, 4.0])
+@pytest.mark.parametrize("decay_shift", [0.0, 4.0, -4.0, -10.0])
 def test_c0_shape_bf16_many_rounds(decay_shift):
+    """decay_shift > 0: weak decays; < 0: strong ones, down to decays that
+    underflow to exactly 0 in fp32 (the fold then restarts from the record's
+    own outer product, and its running decay factor is renormalised often)."""
     wl = gen.Workload("tiny-bf16", B=3, H=2, HV=4, K=32, V=32, T=4, L=16, io_dtype=gen.BF16,
                       prefix=16)
     sc = Scenario(wl, B=3, seed=1, num_slots=6, decay_shift=decay_shift)
