@@ -472,7 +472,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 const float bi = row_live ? betaS[i] : 0.0f;
                 float c = 1.0f;
 #pragma unroll 1
-                for (int cc = kLMax / 16 - 1; cc >= 0; --cc) {  // key columns, high chunk first
+                // key columns below n (the bound is the same in every thread),
+                // high chunk first
+                for (int cc = (n + 15) / 16 - 1; cc >= 0; --cc) {
                     float gk[16];
                     ptx::tmem_ld16(tbase + 16 * cc, gk);
                     ptx::tmem_ld_wait();
