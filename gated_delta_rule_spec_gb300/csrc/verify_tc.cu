@@ -523,14 +523,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             if (!waited && tid == 0) misc[5] = 1;
             __syncthreads();
 
-            // ---- 4. M (I + A) = F^T, all T rows in warp 0; lane l ends with M[s][l],
-            //         M[s][l+32].  Meanwhile one thread of warp 1 fetches the next unit.
-            if (warp == 0) {
-                float f0[TM], f1[TM];
+            // ---- 4. M (I + A) = F^T: the T right-hand sides are independent
+            //         systems, s in warp s % 4; lane l ends with M[s][l], M[s][l+32]
+            {
+                constexpr int SPW = (TM + 3) / 4;   // right-hand sides per warp
+                float f0[SPW], f1[SPW];
 #pragma unroll
-                for (int s = 0; s < TM; ++s) {
-                    f0[s] = lane < n ? F[lane * TM + s] : 0.0f;
-                    f1[s] = lane + 32 < n ? F[(lane + 32) * TM + s] : 0.0f;
+                for (int q = 0; q < SPW; ++q) {
+                    const int sq = warp + 4 * q;
+                    f0[q] = (sq < T && lane < n) ? F[lane * TM + sq] : 0.0f;
+                    f1[q] = (sq < T && lane + 32 < n) ? F[(lane + 32) * TM + sq] : 0.0f;
                 }
                 // four tokens j-3..j per step: the 4 x 4 diagonal block is solved
                 // redundantly on every lane, then all lanes apply the four updates
@@ -550,26 +552,26 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                     d[4] = A[(j - 1) * kALd + j - 3];  // A[j-1][j-3]
                     d[5] = A[(j - 2) * kALd + j - 3];  // A[j-2][j-3]
 #pragma unroll
-                    for (int s = 0; s < TM; ++s) {
+                    for (int q = 0; q < SPW; ++q) {
                         float fj[4];
 #pragma unroll
                         for (int qq = 0; qq < 4; ++qq)
-                            fj[qq] = __shfl_sync(0xffffffffu, (j - qq) < 32 ? f0[s] : f1[s], (j - qq) & 31);
+                            fj[qq] = __shfl_sync(0xffffffffu, (j - qq) < 32 ? f0[q] : f1[q], (j - qq) & 31);
                         const float m0 = fj[0];
                         const float m1 = fmaf(-d[0], m0, fj[1]);
                         const float m2 = fmaf(-d[3], m1, fmaf(-d[1], m0, fj[2]));
                         const float m3 = fmaf(-d[5], m2, fmaf(-d[4], m1, fmaf(-d[2], m0, fj[3])));
-                        f0[s] = fmaf(-ar[3][0], m3, fmaf(-ar[2][0], m2, fmaf(-ar[1][0], m1, fmaf(-ar[0][0], m0, f0[s]))));
-                        f1[s] = fmaf(-ar[3][1], m3, fmaf(-ar[2][1], m2, fmaf(-ar[1][1], m1, fmaf(-ar[0][1], m0, f1[s]))));
+                        f0[q] = fmaf(-ar[3][0], m3, fmaf(-ar[2][0], m2, fmaf(-ar[1][0], m1, fmaf(-ar[0][0], m0, f0[q]))));
+                        f1[q] = fmaf(-ar[3][1], m3, fmaf(-ar[2][1], m2, fmaf(-ar[1][1], m1, fmaf(-ar[0][1], m0, f1[q]))));
                     }
                 }
                 for (; j >= 0; --j) {
                     const float a0 = A[j * kALd + lane], a1 = A[j * kALd + 32 + lane];
 #pragma unroll
-                    for (int s = 0; s < TM; ++s) {
-                        const float m = __shfl_sync(0xffffffffu, j < 32 ? f0[s] : f1[s], j & 31);
-                        f0[s] = fmaf(-a0, m, f0[s]);
-                        f1[s] = fmaf(-a1, m, f1[s]);
+                    for (int q = 0; q < SPW; ++q) {
+                        const float m = __shfl_sync(0xffffffffu, j < 32 ? f0[q] : f1[q], j & 31);
+                        f0[q] = fmaf(-a0, m, f0[q]);
+                        f1[q] = fmaf(-a1, m, f1[q]);
                     }
                 }
                 // c = M beta (output) and c eG (effective query), rows j = lane, lane + 32
@@ -577,33 +579,42 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 for (int hlf = 0; hlf < 2; ++hlf) {
                     const int jj = lane + 32 * hlf;
                     const float bj = jj < n ? betaS[jj] : 0.0f, ej = jj < n ? eG[jj] : 0.0f;
-                    float cj[TM], ce[TM];
 #pragma unroll
-                    for (int s = 0; s < TM; ++s) {
-                        cj[s] = (hlf ? f1[s] : f0[s]) * bj;
-                        ce[s] = cj[s] * ej;
-                    }
-#pragma unroll
-                    for (int s = 0; s < TM; s += 4) {
-                        *reinterpret_cast<float4 *>(sm + c_off(jj) + 4 * s) =
-                            make_float4(cj[s], cj[s + 1], cj[s + 2], cj[s + 3]);
-                        *reinterpret_cast<float4 *>(F + jj * TM + s) =
-                            make_float4(ce[s], ce[s + 1], ce[s + 2], ce[s + 3]);
+                    for (int q = 0; q < SPW; ++q) {
+                        const int sq = warp + 4 * q;
+                        if (sq < TM) {
+                            const float cj = (hlf ? f1[q] : f0[q]) * bj;
+                            *reinterpret_cast<float *>(sm + c_off(jj) + 4 * sq) = cj;
+                            F[jj * TM + sq] = cj * ej;
+                        }
                     }
                 }
             }
             __syncthreads();
 
             // ---- 5. the v history of this CTA's rows into the (now dead) A
-            //         matrix: one 1-D bulk copy per record, spread over warp 0
+            //         matrix by 1-D bulk copies: with V = 128 whole records are
+            //         contiguous, so the history is one or two ring segments;
+            //         otherwise one copy per record, spread over warp 0
             if (warp == 0 && W > 0) {
                 ptx::fence_proxy_async_smem();   // the A matrix was last read by generic loads
-                if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)W * kBV * 2);
-                __syncwarp();
-                for (int jj = lane; jj < W; jj += 32)
-                    ptx::bulk_copy_g2s(sm_s + kOffA + jj * kBV * 2,
-                                       rawv + (sh_hv * L + ring_pos(base, jj, L)) * V + v0, kBV * 2,
-                                       bar_vh);
+                if (V == kBV) {
+                    if (lane == 0) {
+                        ptx::mbar_expect_tx(bar_vh, (uint32_t)W * kBV * 2);
+                        const int n1 = (L - base) < W ? (L - base) : W;
+                        ptx::bulk_copy_g2s(sm_s + kOffA, rawv + (sh_hv * L + base) * V, n1 * kBV * 2, bar_vh);
+                        if (W > n1)
+                            ptx::bulk_copy_g2s(sm_s + kOffA + n1 * kBV * 2, rawv + sh_hv * L * V,
+                                               (W - n1) * kBV * 2, bar_vh);
+                    }
+                } else {
+                    if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)W * kBV * 2);
+                    __syncwarp();
+                    for (int jj = lane; jj < W; jj += 32)
+                        ptx::bulk_copy_g2s(sm_s + kOffA + jj * kBV * 2,
+                                           rawv + (sh_hv * L + ring_pos(base, jj, L)) * V + v0, kBV * 2,
+                                           bar_vh);
+                }
             }
             // q_eff (thread = key channel): eG_{W+s} q^_s - sum_j c[j][s] eG_j k^_j
             {
@@ -613,6 +624,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 float acc[TM];
 #pragma unroll
                 for (int s = 0; s < TM; ++s) acc[s] = 0.0f;
+#pragma unroll 4
                 for (int j = 0; j < n; ++j) {
                     const float x = *reinterpret_cast<const float *>(sm + xbase + j * 128 + ((kch ^ (j & 7)) << 4));
 #pragma unroll
@@ -652,6 +664,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 ph_vh ^= 1u;
             }
             if (vrow < V) {
+#pragma unroll 4
                 for (int j = 0; j < W; ++j) {
                     const float x = __bfloat162float(vh[j * kBV + tid]);
 #pragma unroll
