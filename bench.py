@@ -185,8 +185,9 @@ class Workload:
         return d
 
 
-def build_state(wl: Workload, seed: int, device):
-    """Layer state built by the library's own rounds from a zero checkpoint."""
+def build_state(wl: Workload, seed: int, device, random_rounds: int = 48):
+    """Layer state built by the library's own rounds from a zero checkpoint:
+    16 full-accept rounds, then random_rounds with accept_len ~ U{1..T}."""
     import torch
     from gated_delta_rule_spec_gb300 import binding
     from gated_delta_rule_spec_gb300 import inputs as gen
@@ -206,7 +207,7 @@ def build_state(wl: Workload, seed: int, device):
 
     binding.reset(cur, slots)
     full = torch.full((wl.B,), wl.T, dtype=torch.int32, device=device)
-    for r in range(16 + 48):
+    for r in range(16 + random_rounds):
         w = dev_window()
         binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias)
         acc = full if r < 16 else torch.from_numpy(gen.accept_lens(rng, wl.B, wl.T)).to(device)
@@ -227,7 +228,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     device = torch.device("cuda", local)
     binding.load()
     wl = Workload(args.batch)
-    rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 1000 + rank, device)
+    rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 1000 + rank, device,
+                                                                     args.setup_rounds)
     path = binding.verify_path(layer)
 
     NI = 16
@@ -326,37 +328,82 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         for Wr in W_last]))
     mean_W = float(W_last.mean())
 
-    # e2e through the binding with host buffers: H2D inputs, D2H outputs, every step
-    host_in = [{n: t.cpu().pin_memory() for n, t in inputs[i].items()} for i in range(4)]
-    host_acc = torch.from_numpy(acc_np).pin_memory()
-    host_out = torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16).pin_memory()
-    dev_in = {n: torch.empty_like(t) for n, t in inputs[0].items()}
-    dev_acc = torch.empty(wl.B, dtype=torch.int32, device=device)
-    dev_out = torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device)
-    h2d = sum(t.numel() * t.element_size() for t in host_in[0].values()) + wl.B * 4
-    d2h = host_out.numel() * host_out.element_size()
+    # e2e through the binding with host buffers: every step copies its inputs
+    # (q, k, v, a, b and accept_len, packed in one pinned buffer) to the device
+    # and its output back.  The transfers overlap the previous and next steps'
+    # kernels as in a serving loop: H2D one step ahead on a copy stream, D2H on
+    # another, device buffers doubled, events ordering every reuse.
+    names = ["q", "k", "v", "a", "b"]
+    shapes = {n: inputs[0][n].shape for n in names}
+    dtypes = {n: inputs[0][n].dtype for n in names}
+    offs, off = {}, 0
+    for n in names:
+        offs[n] = off
+        off += (inputs[0][n].numel() * inputs[0][n].element_size() + 255) // 256 * 256
+    offs["acc"] = off
+    flat_bytes = off + wl.B * 4
+
+    def views(flat):
+        vw = {n: flat[offs[n]:offs[n] + inputs[0][n].numel() * inputs[0][n].element_size()]
+              .view(dtypes[n]).view(shapes[n]) for n in names}
+        vw["acc"] = flat[offs["acc"]:offs["acc"] + wl.B * 4].view(torch.int32)
+        return vw
+
+    host_flat = [torch.empty(flat_bytes, dtype=torch.uint8).pin_memory() for _ in range(4)]
+    for i in range(4):
+        hv_ = views(host_flat[i])
+        for n in names:
+            hv_[n].copy_(inputs[i][n].cpu())
+        hv_["acc"].copy_(torch.from_numpy(acc_np[i % R]))
+    dev_flat = [torch.empty(flat_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    dev_v = [views(f) for f in dev_flat]
+    dev_out = [torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device) for _ in range(2)]
+    host_out = [torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h2d = flat_bytes
+    d2h = host_out[0].numel() * host_out[0].element_size()
     K_e2e = max(3, min(args.steps, 200))
+    comp = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]   # a step's inputs consumed
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # a step's output written
+    ev_read = [torch.cuda.Event() for _ in range(2)]   # a step's output copied out
 
-    def e2e_step(i):
-        src = host_in[i % 4]
-        for n in dev_in:
-            dev_in[n].copy_(src[n], non_blocking=True)
-        dev_acc.copy_(host_acc[i % R], non_blocking=True)
-        binding.verify(layer, cur, slots, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["a"],
-                       dev_in["b"], A_log, dt_bias, out=dev_out)
-        binding.commit(cur, wl.T, wl.L, slots, dev_acc)
-        binding.fold(layer, cur, slots)
-        host_out.copy_(dev_out, non_blocking=True)
+    def upload(i):
+        buf = i % 2
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(ev_free[buf])
+            dev_flat[buf].copy_(host_flat[i % 4], non_blocking=True)
+            ev_in[buf].record(h2d_s)
 
-    for i in range(3):
-        e2e_step(i)
+    def run_e2e(n_steps):
+        upload(0)
+        for i in range(n_steps):
+            if i + 1 < n_steps:
+                upload(i + 1)
+            buf = i % 2
+            d = dev_v[buf]
+            comp.wait_event(ev_in[buf])
+            comp.wait_event(ev_read[buf])
+            binding.verify(layer, cur, slots, d["q"], d["k"], d["v"], d["a"], d["b"], A_log, dt_bias,
+                           out=dev_out[buf])
+            binding.commit(cur, wl.T, wl.L, slots, d["acc"])
+            ev_free[buf].record(comp)
+            binding.fold(layer, cur, slots)
+            ev_out[buf].record(comp)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_out[buf])
+                host_out[buf].copy_(dev_out[buf], non_blocking=True)
+                ev_read[buf].record(d2h_s)
+        comp.wait_stream(d2h_s)
+
+    run_e2e(3)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(K_e2e):
-        e2e_step(i)
+    run_e2e(K_e2e)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -380,7 +427,9 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         "config": wl.config({"verify_kernel": path, "mean_ring_fill_W": round(mean_W, 2)}),
         "e2e": {"value": round(world * wl.B * wl.T * K_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "steps": K_e2e, "api": "python binding -> C ABI, host pinned buffers"},
+                "steps": K_e2e,
+                "api": "python binding -> C ABI, host pinned buffers; transfers overlap the "
+                       "neighbouring steps' kernels (copy streams, double buffers)"},
         "gpu_launches": 4 * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -532,6 +581,8 @@ def main():
     ap.add_argument("--batch", type=int, default=128)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--setup-rounds", type=int, default=48,
+                    help="random rounds of the state build (fewer: a short run to profile)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
