@@ -26,6 +26,7 @@ on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -80,9 +81,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(path_name: str, B: int):
+def profiled_traffic(path_name: str, B: int, T: int):
     """DRAM bytes per verify launch from the committed ncu summary, if it was
-    taken on the current verify source; else None."""
+    taken on the current verify source and the same window; else None."""
     f = os.path.join(ROOT, "profiles", f"verify_{path_name}_traffic.json")
     if not os.path.exists(f):
         return None
@@ -90,7 +91,7 @@ def profiled_traffic(path_name: str, B: int):
         rec = json.load(open(f))
     except Exception:
         return None
-    if rec.get("kernel_source_hash") != kernel_source_hash():
+    if rec.get("kernel_source_hash") != kernel_source_hash() or rec.get("T") != T:
         return None
     per_row = rec.get("dram_bytes_per_launch_per_row")
     return None if per_row is None else float(per_row) * B
@@ -163,11 +164,15 @@ class ClockSampler:
 # ----------------------------------------------------------------- our arm
 
 class Workload:
-    def __init__(self, B: int):
+    def __init__(self, B: int, T: int | None = None):
+        """The Qwen3-Next-shaped layer at B rows; T = 1 is plain decode (a window
+        of one token through the same calls, checkpoint, ring and cursors)."""
         from gated_delta_rule_spec_gb300 import inputs as gen
         c = gen.WORKLOADS["C2"]
-        self.name = f"qwen3next-gdn-verify-b{B}"
-        self.B, self.H, self.HV, self.K, self.V, self.T, self.L = B, c.H, c.HV, c.K, c.V, c.T, c.L
+        T = c.T if T is None else T
+        self.name = f"qwen3next-gdn-{'decode' if T == 1 else 'verify'}-b{B}" + (
+            f"-t{T}" if T not in (1, c.T) else "")
+        self.B, self.H, self.HV, self.K, self.V, self.T, self.L = B, c.H, c.HV, c.K, c.V, T, c.L
         self.num_slots = max(c.num_slots, B)
         self.G = self.HV // self.H
         self.e = 2
@@ -227,7 +232,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     binding.load()
-    wl = Workload(args.batch)
+    wl = Workload(args.batch, args.window)
     rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 1000 + rank, device,
                                                                      args.setup_rounds)
     path = binding.verify_path(layer)
@@ -418,7 +423,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     peaks, peak_kind = measured_peaks()
     v_ms = float(np.mean(verify_ms)) if verify_ms else float("nan")
     achieved = bytes_per_launch / (v_ms / 1e3) / 1e9 if verify_ms else float("nan")
-    traffic = profiled_traffic(path, wl.B)
+    traffic = profiled_traffic(path, wl.B, wl.T)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
@@ -478,13 +483,15 @@ def verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias, 
     return [statistics.median(times)]
 
 
-def cpu_baseline(B: int, seconds: float = 10.0) -> dict:
+def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None) -> dict:
     """The fp64 oracle, as it stands, on the host cores: verify of a sample of
     the workload's rows (all heads), ring fill W ~ U[0, L-2T] as in the sweep."""
     import oracle
     from gated_delta_rule_spec_gb300 import inputs as gen
 
     c = gen.WORKLOADS["C2"]
+    if T is not None and T != c.T:
+        c = dataclasses.replace(c, T=T)
     rows = min(B, 16)
     rng = gen.rng_for(7, "cpu-baseline", rows)
     d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
@@ -524,8 +531,8 @@ def run_reference(args, rank: int, world: int) -> dict | None:
     import oracle
     from gated_delta_rule_spec_gb300 import inputs as gen
 
-    wl = Workload(args.batch)
-    c = gen.WORKLOADS["C2"]
+    wl = Workload(args.batch, args.window)
+    c = dataclasses.replace(gen.WORKLOADS["C2"], T=wl.T)
     rows = 2
     rng = gen.rng_for(11, "reference-arm", rows)
     d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
@@ -581,6 +588,8 @@ def main():
     ap.add_argument("--batch", type=int, default=128)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--window", type=int, default=None,
+                    help="draft window T (default: the workload's 4; 1 = plain decode)")
     ap.add_argument("--setup-rounds", type=int, default=48,
                     help="random rounds of the state build (fewer: a short run to profile)")
     args = ap.parse_args()
@@ -600,7 +609,7 @@ def main():
     else:
         line = run_ours(args, rank, world)
         if line is not None and world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args.batch)
+            line["cpu_baseline"] = cpu_baseline(args.batch, T=args.window)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
