@@ -38,6 +38,7 @@ ST_ACCEPT_RANGE = 1
 ST_SLOT_OOR = 2
 ST_RING_OVERFLOW = 4
 ST_CURSOR_CORRUPT = 8
+ST_UNFOLDED = 32
 
 _lib = None
 
@@ -107,6 +108,9 @@ def _load(path: str | None = None):
         _lib.orc_fold.argtypes = [P, P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int]
         _lib.orc_reset.restype = ctypes.c_uint32
         _lib.orc_reset.argtypes = [P, P, P, ctypes.c_int]
+        _lib.orc_prefill.restype = ctypes.c_uint32
+        _lib.orc_prefill.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int] + [P] * 8 + [
+            ctypes.c_int, ctypes.c_int]
         _lib.orc_run.restype = None
         _lib.orc_run.argtypes = [P, P, ctypes.c_int, P, P, P, P]
         _lib.orc_run_batch.restype = None
@@ -317,6 +321,26 @@ def fold(dims: Dims, layers, cursors: Cursors, slot_idx, nthreads: int = 1) -> i
     cd, cc = dims._c(), cursors._c()
     return int(_load().orc_fold(ctypes.byref(cd), arr, len(layers), ctypes.byref(cc),
                                 _ptr(slot_idx), slot_idx.shape[0], int(nthreads)))
+
+
+def prefill(dims: Dims, layer: Layer, cursors: Cursors, slot_idx, q, k, v, a, b, A_log, dt_bias,
+            from_zero: bool = True, nthreads: int = 1):
+    """Prefill of N prompt tokens per row: returns (out [B, N, HV, V] fp64, status
+    bits).  The final states replace the rows' checkpoints and the rows' cursors
+    are reset.  q, k [B, N, H, K]; v [B, N, HV, V]; a, b [B, N, HV] (KDA a
+    [B, N, HV, K]).  ``from_zero=False`` continues from the checkpoint and needs
+    an empty ring (write_pos 0), else the row is skipped with ST_UNFOLDED."""
+    slot_idx = _i32(slot_idx)
+    B = slot_idx.shape[0]
+    q, k, v, a, b = _f64(q), _f64(k), _f64(v), _f64(a), _f64(b)
+    A_log, dt_bias = _f64(A_log), _f64(dt_bias)
+    N = q.shape[1]
+    out = np.zeros((B, N, dims.HV, dims.V), np.float64)
+    cd, cl, cc = dims._c(), layer._c(), cursors._c()
+    st = _load().orc_prefill(ctypes.byref(cd), ctypes.byref(cl), ctypes.byref(cc), _ptr(slot_idx),
+                             B, N, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                             _ptr(dt_bias), _ptr(out), int(bool(from_zero)), int(nthreads))
+    return out, int(st)
 
 
 def reset(dims: Dims, cursors: Cursors, slot_idx) -> int:

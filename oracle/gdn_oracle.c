@@ -53,6 +53,7 @@
 #define ORC_ST_SLOT_OOR       2u
 #define ORC_ST_RING_OVERFLOW  4u
 #define ORC_ST_CURSOR_CORRUPT 8u
+#define ORC_ST_UNFOLDED      32u   /* prefill from the checkpoint with records not yet folded */
 
 typedef struct {
     int H, HV, K, V, T, L, num_slots;
@@ -514,4 +515,114 @@ void orc_run_batch(const orc_dims *d, int nunits, double *S, int n, const double
     for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
     free(th);
     pthread_mutex_destroy(&J.lock);
+}
+
+/* ------------------------------------------------------------------ */
+/* Prefill: the recurrence over the N prompt tokens of every row, with   */
+/* the output of every token, from a zero state or from the row's        */
+/* checkpoint; the final state becomes the checkpoint and the row's      */
+/* cursors are reset for decode (the prefill -> decode handoff, [blog]   */
+/* appendix A.2).  Continuing from the checkpoint needs an empty ring    */
+/* (write_pos == 0): the committed state is then the checkpoint itself.  */
+/* ------------------------------------------------------------------ */
+
+typedef struct {
+    const orc_dims *d;
+    orc_layer *ly;
+    const orc_cursors *cur;
+    const int32_t *slot_idx;
+    int B, N, from_zero;
+    const double *q, *k, *v, *a, *b, *A_log, *dt_bias;
+    double *out;
+    int next_unit;
+    pthread_mutex_t lock;
+} prefill_job;
+
+/* Which rows a prefill computes; sets the status bits of the others. */
+static int prefill_row_ok(const orc_dims *d, const orc_cursors *cur, int slot, int from_zero,
+                          uint32_t *st)
+{
+    if (slot < 0) return 0;
+    if (slot >= d->num_slots) { *st |= ORC_ST_SLOT_OOR; return 0; }
+    int wp = cur->write_pos[slot], base = cur->cache_base[slot];
+    if (wp < 0 || wp > d->L || base < 0 || base >= d->L) { *st |= ORC_ST_CURSOR_CORRUPT; return 0; }
+    if (!from_zero && wp != 0) { *st |= ORC_ST_UNFOLDED; return 0; }
+    return 1;
+}
+
+static void prefill_unit(prefill_job *J, int bb, int hv)
+{
+    const orc_dims *d = J->d;
+    const int K = d->K, V = d->V, N = J->N, H = d->H, HV = d->HV;
+    const int h = hv / (HV / H);
+    int slot = J->slot_idx[bb];
+    uint32_t st = 0;
+    if (!prefill_row_ok(d, J->cur, slot, J->from_zero, &st)) {
+        for (int t = 0; t < N; ++t)
+            memset(J->out + (((size_t)bb * N + t) * HV + hv) * V, 0, sizeof(double) * V);
+        return;
+    }
+    const size_t gw = g_width(d);
+    double *S = J->ly->checkpoint + ((size_t)slot * HV + hv) * V * K;
+    double *g = (double *)malloc(sizeof(double) * gw);
+    if (J->from_zero) memset(S, 0, sizeof(double) * (size_t)V * K);
+    for (int t = 0; t < N; ++t) {
+        size_t tok = (size_t)bb * N + t;
+        if (d->per_key_gate) {
+            for (int j = 0; j < K; ++j)
+                g[j] = orc_gate_g(J->A_log[hv], J->a[(tok * HV + hv) * K + j], J->dt_bias[(size_t)hv * K + j]);
+        } else {
+            g[0] = orc_gate_g(J->A_log[hv], J->a[tok * HV + hv], J->dt_bias[hv]);
+        }
+        double beta = orc_gate_beta(J->b[tok * HV + hv]);
+        orc_step(V, K, d->per_key_gate, S, J->v + (tok * HV + hv) * V, J->k + (tok * H + h) * K, g,
+                 beta, d->l2_eps);
+        orc_readout(V, K, S, J->q + (tok * H + h) * K, d->l2_eps, d->scale, J->out + (tok * HV + hv) * V);
+    }
+    free(g);
+}
+
+static void *prefill_worker(void *arg)
+{
+    prefill_job *J = (prefill_job *)arg;
+    const int nunits = J->B * J->d->HV;
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int u = J->next_unit++;
+        pthread_mutex_unlock(&J->lock);
+        if (u >= nunits) break;
+        prefill_unit(J, u / J->d->HV, u % J->d->HV);
+    }
+    return NULL;
+}
+
+/* q, k: [B, N, H, K]; v: [B, N, HV, V]; a: [B, N, HV] (per-key gate: [B, N, HV, K]);
+ * b: [B, N, HV]; out: [B, N, HV, V].  Returns the OR of the rows' status bits. */
+uint32_t orc_prefill(const orc_dims *d, orc_layer *ly, orc_cursors *cur, const int32_t *slot_idx,
+                     int B, int N, const double *q, const double *k, const double *v,
+                     const double *a, const double *b, const double *A_log, const double *dt_bias,
+                     double *out, int from_zero, int nthreads)
+{
+    prefill_job J;
+    memset(&J, 0, sizeof J);
+    J.d = d; J.ly = ly; J.cur = cur; J.slot_idx = slot_idx; J.B = B; J.N = N; J.from_zero = from_zero;
+    J.q = q; J.k = k; J.v = v; J.a = a; J.b = b; J.A_log = A_log; J.dt_bias = dt_bias; J.out = out;
+    pthread_mutex_init(&J.lock, NULL);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, prefill_worker, &J);
+    prefill_worker(&J);
+    for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    pthread_mutex_destroy(&J.lock);
+    /* the cursors of the rows computed are reset for decode */
+    uint32_t st = 0;
+    for (int bb = 0; bb < B; ++bb) {
+        int slot = slot_idx[bb];
+        if (!prefill_row_ok(d, cur, slot, from_zero, &st)) continue;
+        cur->write_pos[slot] = 0;
+        cur->cache_base[slot] = 0;
+        cur->is_flush[slot] = 0;
+    }
+    return st;
 }
