@@ -22,6 +22,7 @@ from . import build as _build
 GATE_SCALAR, GATE_PER_KEY = 0, 1
 DTYPE_BF16, DTYPE_FP32 = 0, 1
 ST_ACCEPT_RANGE, ST_SLOT_OOR, ST_RING_OVERFLOW, ST_CURSOR_CORRUPT, ST_TIMEOUT = 1, 2, 4, 8, 16
+ST_UNFOLDED = 32
 
 _IO_TORCH = {DTYPE_BF16: torch.bfloat16, DTYPE_FP32: torch.float32}
 _NAME_TO_DTYPE = {"bf16": DTYPE_BF16, "fp32": DTYPE_FP32}
@@ -48,7 +49,7 @@ class CursorDesc(ctypes.Structure):
 
 
 _lib = None
-EXPORTS = ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset",
+EXPORTS = ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset", "gdn_spec_prefill",
            "gdn_spec_read_status", "gdn_spec_strerror", "gdn_spec_abi_version",
            "gdn_spec_verify_path")
 
@@ -74,9 +75,10 @@ def load() -> ctypes.CDLL:
     lib.gdn_spec_commit.argtypes = [CP, I32, I32, P, I32, P, P]
     lib.gdn_spec_fold.argtypes = [LP, I32, CP, P, I32, P]
     lib.gdn_spec_reset.argtypes = [CP, P, I32, P]
+    lib.gdn_spec_prefill.argtypes = [LP, CP, P, I32, I32, P, P, P, P, P, P, P, P, I32, P]
     lib.gdn_spec_read_status.argtypes = [CP, ctypes.POINTER(ctypes.c_uint32), I32, P]
     for name in ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset",
-                 "gdn_spec_read_status"):
+                 "gdn_spec_prefill", "gdn_spec_read_status"):
         getattr(lib, name).restype = ctypes.c_int
     lib.gdn_spec_strerror.argtypes = [ctypes.c_int]
     lib.gdn_spec_strerror.restype = ctypes.c_char_p
@@ -206,6 +208,33 @@ def fold(layers, cursors: SpecCursors, slot_idx: torch.Tensor, stream=None) -> N
     rc = load().gdn_spec_fold(arr, len(layers), ctypes.byref(cursors.desc()), _ptr(slot_idx), B,
                               _stream(stream))
     _check(rc, "gdn_spec_fold")
+
+
+def prefill(layer: SpecLayer, cursors: SpecCursors, slot_idx: torch.Tensor, q, k, v, a, b,
+            A_log, dt_bias, out: torch.Tensor | None = None, from_zero: bool = True,
+            stream=None) -> torch.Tensor:
+    """gdn_spec_prefill: outputs of the N prompt tokens [B, N, HV, V]; the final
+    states become the slots' checkpoints and the slots' cursors are reset."""
+    B = slot_idx.shape[0]
+    N = q.shape[1]
+    T, H, HV, K, V = N, layer.H, layer.HV, layer.K, layer.V
+    io = layer.io_torch
+    _need(slot_idx, "slot_idx", torch.int32, (B,))
+    shp = {"q": (B, T, H, K), "k": (B, T, H, K), "v": (B, T, HV, V),
+           "a": (B, T, HV, K) if layer.per_key_gate else (B, T, HV), "b": (B, T, HV)}
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need(t, name, io, shp[name])
+    _need(A_log, "A_log", torch.float32, (HV,))
+    _need(dt_bias, "dt_bias", torch.float32, (HV, K) if layer.per_key_gate else (HV,))
+    if out is None:
+        out = torch.empty((B, N, HV, V), dtype=io, device=q.device)
+    _need(out, "out", io, (B, N, HV, V))
+    rc = load().gdn_spec_prefill(ctypes.byref(layer.desc()), ctypes.byref(cursors.desc()),
+                                 _ptr(slot_idx), B, N, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                 _ptr(A_log), _ptr(dt_bias), _ptr(out), int(bool(from_zero)),
+                                 _stream(stream))
+    _check(rc, "gdn_spec_prefill")
+    return out
 
 
 def reset(cursors: SpecCursors, slot_idx: torch.Tensor, stream=None) -> None:

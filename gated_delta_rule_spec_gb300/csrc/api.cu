@@ -28,6 +28,11 @@ cudaError_t launch_commit(const CursorArgs &C, int T, int L, const int32_t *slot
 cudaError_t launch_fold_cursors(const CursorArgs &C, int L, const int32_t *slot_idx, int B,
                                 cudaStream_t stream);
 cudaError_t launch_reset(const CursorArgs &C, const int32_t *slot_idx, int B, cudaStream_t stream);
+cudaError_t launch_prefill(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
+                           const int32_t *slot_idx, int B, int N, const void *q, const void *k,
+                           const void *v, const void *a, const void *b, const float *A_log,
+                           const float *dt_bias, void *out, int from_zero, cudaStream_t stream);
+size_t prefill_smem_bytes(int K, bool kda, bool bf16);
 }  // namespace gdnspec
 
 using namespace gdnspec;
@@ -194,6 +199,28 @@ int gdn_spec_fold(const gdn_spec_layer *layers, int32_t n_layers, const gdn_spec
         if ((rc = cuda_rc(launch_fold(P, FL, cnt, kda, bf16, C, slot_idx, B, st)))) return rc;
     }
     return cuda_rc(launch_fold_cursors(C, P.L, slot_idx, B, st));
+}
+
+int gdn_spec_prefill(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
+                     const int32_t *slot_idx, int32_t B, int32_t N, const void *q, const void *k,
+                     const void *v, const void *a, const void *b, const float *A_log,
+                     const float *dt_bias, void *out, int32_t from_zero, void *stream) {
+    int rc = check_layer(layer);
+    if (rc) return rc;
+    if ((rc = check_cursors(cursors))) return rc;
+    if (cursors->num_slots != layer->num_slots) return GDN_SPEC_EINVAL;
+    if (B < 0 || N < 0) return GDN_SPEC_EINVAL;
+    if (B == 0) return GDN_SPEC_OK;
+    if (!slot_idx) return GDN_SPEC_EINVAL;
+    if (N > 0 && (!q || !k || !v || !a || !b || !A_log || !dt_bias || !out)) return GDN_SPEC_EINVAL;
+    if (N > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)))
+        return GDN_SPEC_EALIGN;
+    const bool kda = layer->gate_kind == GDN_SPEC_GATE_PER_KEY;
+    const bool bf16 = layer->io_dtype == GDN_SPEC_DTYPE_BF16;
+    if (prefill_smem_bytes(layer->K, kda, bf16) > kMaxSmem) return GDN_SPEC_EUNSUPPORTED;
+    return cuda_rc(launch_prefill(layer_args(layer), cursor_args(cursors), kda, bf16, slot_idx, B, N,
+                                  q, k, v, a, b, A_log, dt_bias, out, from_zero ? 1 : 0,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_spec_reset(const gdn_spec_cursors *cursors, const int32_t *slot_idx, int32_t B,

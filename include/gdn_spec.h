@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define GDN_SPEC_ABI_VERSION 1
+#define GDN_SPEC_ABI_VERSION 2   /* 2: adds gdn_spec_prefill */
 
 /* host-side error codes (return values) */
 #define GDN_SPEC_OK            0
@@ -82,6 +82,7 @@ extern "C" {
 #define GDN_SPEC_ST_RING_OVERFLOW  4u  /* verify: write_pos + T > L (a fold was skipped)  */
 #define GDN_SPEC_ST_CURSOR_CORRUPT 8u  /* write_pos < 0, write_pos > L or cache_base outside [0, L) */
 #define GDN_SPEC_ST_TIMEOUT       16u  /* a bounded device wait ran out (that call's outputs are invalid) */
+#define GDN_SPEC_ST_UNFOLDED      32u  /* prefill: continuing from a checkpoint whose ring is not folded */
 
 #define GDN_SPEC_GATE_SCALAR  0    /* GDN: one gate per (token, v-head)            */
 #define GDN_SPEC_GATE_PER_KEY 1    /* KDA: one gate per (token, v-head, key channel) */
@@ -183,6 +184,33 @@ int gdn_spec_fold(const gdn_spec_layer *layers, int32_t n_layers,
  */
 int gdn_spec_reset(const gdn_spec_cursors *cursors, const int32_t *slot_idx, int32_t B,
                    void *stream);
+
+/*
+ * gdn_spec_prefill -- prefill of each row's N prompt tokens into its slot
+ * (the step before decode; the reset of the prefill -> decode handoff,
+ * [blog] appendix A.2, is part of it): for every v-head the recurrence runs
+ * over the tokens, token by token in fp32 as the fold does, from a zero
+ * state (from_zero != 0) or from the slot's checkpoint (from_zero == 0, which
+ * gives chunked prefill across calls); every token's output is written, the
+ * final state becomes the slot's checkpoint, and the slot's cursors are reset
+ * (write_pos = cache_base = is_flush = 0).  The ring is not written.
+ *   q, k      io_dtype [B, N, H, K]
+ *   v         io_dtype [B, N, HV, V]
+ *   a         io_dtype [B, N, HV]   (GATE_PER_KEY: [B, N, HV, K])
+ *   b         io_dtype [B, N, HV]
+ *   A_log     fp32 [HV];  dt_bias fp32 [HV] (GATE_PER_KEY: [HV, K])
+ *   out       io_dtype [B, N, HV, V]  (written)
+ * N >= 0 (N = 0 only zeroes the checkpoints when from_zero, and resets).
+ * Device status: SLOT_OOR, CURSOR_CORRUPT, and UNFOLDED when from_zero == 0
+ * and the slot's write_pos is not 0 (committed records not yet folded: fold
+ * them first); such a row is skipped (its checkpoint and cursors untouched,
+ * its outputs zero).
+ */
+int gdn_spec_prefill(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
+                     const int32_t *slot_idx, int32_t B, int32_t N,
+                     const void *q, const void *k, const void *v, const void *a,
+                     const void *b, const float *A_log, const float *dt_bias, void *out,
+                     int32_t from_zero, void *stream);
 
 /*
  * gdn_spec_read_status -- copy the device status word to *host_out after

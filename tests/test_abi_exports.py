@@ -64,6 +64,7 @@ def test_python_constants_match_header():
     assert d["GDN_SPEC_ST_RING_OVERFLOW"] == binding.ST_RING_OVERFLOW
     assert d["GDN_SPEC_ST_CURSOR_CORRUPT"] == binding.ST_CURSOR_CORRUPT
     assert d["GDN_SPEC_ST_TIMEOUT"] == binding.ST_TIMEOUT
+    assert d["GDN_SPEC_ST_UNFOLDED"] == binding.ST_UNFOLDED
 
 
 def test_descriptor_layout_matches_header():
