@@ -521,6 +521,161 @@ def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None) -> dict:
                       f"{reps} repetitions in {el:.1f} s, W ~ U[0, {c.L - 2 * c.T}]"}
 
 
+# ----------------------------------------------------------------- prefill
+
+PREFILL_METRIC = "prefilled tokens/s per GDN layer, 1\u00d7GB300"
+
+
+def _prefill_flops(B: int, N: int, wl: "Workload") -> float:
+    """Algorithmic flops of one prefill call: per token and v-head the delta
+    (S k, 2VK), the rank-1 update (2VK) and the output (S q, 2VK)."""
+    return 6.0 * wl.V * wl.K * B * N * wl.HV
+
+
+def run_prefill(args, rank: int, world: int) -> dict | None:
+    """gdn_spec_prefill of B prompts of N tokens (from a zero state) on the
+    Qwen3-Next-shaped layer, timed in CUDA graphs, plus an end-to-end leg
+    (pinned host prompts in, outputs out, every call)."""
+    import torch
+    from gated_delta_rule_spec_gb300 import binding
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    wl = Workload(args.batch)
+    B, N = wl.B, args.prefill
+    rng = gen.rng_for(3000 + rank, "prefill", B)
+    layer = binding.SpecLayer(wl.H, wl.HV, wl.K, wl.V, wl.T, wl.L, wl.num_slots, device=device)
+    cur = binding.SpecCursors(wl.num_slots, device=device)
+    A_log, dt_bias = (torch.from_numpy(x).to(device) for x in gen.layer_params(rng, wl.HV, wl.K, False))
+    slots = torch.from_numpy(gen.scattered_slots(rng, wl.num_slots, B)).to(device)
+    host = gen.window_inputs(rng, B, N, wl.H, wl.HV, wl.K, wl.V, gen.BF16)
+    w = {n: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device) for n, x in host.items()}
+    out = torch.empty(B, N, wl.HV, wl.V, dtype=torch.bfloat16, device=device)
+
+    def call(ins, o):
+        binding.prefill(layer, cur, slots, ins["q"], ins["k"], ins["v"], ins["a"], ins["b"], A_log,
+                        dt_bias, out=o, from_zero=True)
+
+    for _ in range(args.warmup):
+        call(w, out)
+    R = max(1, min(args.steps, 10))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(R):
+                call(w, out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    reps = max(1, (args.steps + R - 1) // R)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    calls = reps * R
+
+    # end to end: prompts from pinned host memory in, outputs out, every call
+    hin = {n: t.cpu().pin_memory() for n, t in w.items()}
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    din = {n: torch.empty_like(t) for n, t in w.items()}
+    K_e2e = max(3, min(args.steps, 20))
+
+    def e2e_call():
+        for n in din:
+            din[n].copy_(hin[n], non_blocking=True)
+        call(din, out)
+        hout.copy_(out, non_blocking=True)
+
+    e2e_call()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K_e2e):
+        e2e_call()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        ms, e2e_ms = reduce_max([ms, e2e_ms], device)
+    if rank != 0:
+        return None
+    t_call = ms / 1e3 / calls
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peaks, _ = measured_peaks()
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12    # fp32 FMA lanes x 2 flops x clock, TFLOP/s
+    achieved = _prefill_flops(B, N, wl) / t_call / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    return {
+        "metric": PREFILL_METRIC, "value": round(world * B * N / t_call, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": calls, "warmup": args.warmup, "ms_per_step": round(ms / calls, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
+        "config": {"workload": f"qwen3next-gdn-prefill-b{B}-n{N}", "B": B, "N": N, "H": wl.H,
+                   "HV": wl.HV, "K": wl.K, "V": wl.V, "io_dtype": "bf16", "state_dtype": "fp32",
+                   "step": "prefill from a zero state (outputs, checkpoint, cursor reset)",
+                   "parallelism": "replicas"},
+        "e2e": {"value": round(world * B * N * K_e2e / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(hout.numel() * hout.element_size()), "steps": K_e2e,
+                "api": "python binding -> C ABI, host pinned buffers"},
+        "gpu_launches": 2 * calls,
+        "roofline": {"bound": "alu", "achieved": round(achieved, 2),
+                     "peak": round(alu_peak, 2), "unit": "TFLOP/s",
+                     "frac": round(achieved / alu_peak, 4), "traffic": None,
+                     "kernel": "prefill", "peak_kind": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
+                     "us_per_call": round(t_call * 1e6, 2)},
+        "clocks": clocks,
+    }
+
+
+def prefill_cpu(B: int, N: int, seconds: float = 10.0) -> dict:
+    """The fp64 oracle's prefill, as it stands, on the host cores, on a sample
+    of the workload (2 rows, all v-heads, the first 32 tokens of each prompt)."""
+    import oracle
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    c = gen.WORKLOADS["C2"]
+    rows, n = min(B, 2), min(N, 32)
+    rng = gen.rng_for(9, "prefill-cpu", rows)
+    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
+    ly = oracle.Layer(d)
+    w = {x: gen.to_f64(y) for x, y in
+         gen.window_inputs(rng, rows, n, c.H, c.HV, c.K, c.V, gen.BF16).items()}
+    A_log, dt = (x.astype(np.float64) for x in gen.layer_params(rng, c.HV, c.K, False))
+    cores = os.cpu_count() or 1
+    slots = np.arange(rows, dtype=np.int32)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        cur = oracle.Cursors(rows)
+        oracle.prefill(d, ly, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
+                       from_zero=True, nthreads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= 1000:
+            break
+    return {"value": round(rows * n * reps / el, 2), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{rows} prompts x {n} tokens x {c.HV} v-heads of the B={B}, N={N} workload, "
+                      f"fp64 prefill, {reps} repetitions in {el:.1f} s"}
+
 # ----------------------------------------------------------------- reference arm
 
 def run_reference(args, rank: int, world: int) -> dict | None:
@@ -590,6 +745,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=None,
                     help="draft window T (default: the workload's 4; 1 = plain decode)")
+    ap.add_argument("--prefill", type=int, default=0, metavar="N",
+                    help="measure gdn_spec_prefill of --batch prompts of N tokens instead")
     ap.add_argument("--setup-rounds", type=int, default=48,
                     help="random rounds of the state build (fewer: a short run to profile)")
     args = ap.parse_args()
@@ -604,7 +761,23 @@ def main():
         if args.impl == "reference":
             backend = "gloo"
         dist.init_process_group(backend)
-    if args.impl == "reference":
+    if args.prefill and args.impl == "reference":
+        line = None
+        if rank == 0:   # the oracle's prefill on the host cores, a bounded sample
+            cb = prefill_cpu(args.batch, args.prefill, seconds=5.0)
+            line = {"impl": "reference", "metric": PREFILL_METRIC, "value": cb["value"],
+                    "unit": cb["unit"], "n_gpus": world, "steps": 1, "warmup": args.warmup,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "f64", "data": "synthetic",
+                    "config": {"workload": f"qwen3next-gdn-prefill-b{args.batch}-n{args.prefill}"},
+                    "cpu_baseline": cb,
+                    "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+    elif args.prefill:
+        line = run_prefill(args, rank, world)
+        if line is not None and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = prefill_cpu(args.batch, args.prefill)
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         line = run_ours(args, rank, world)
