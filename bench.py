@@ -164,13 +164,15 @@ class ClockSampler:
 # ----------------------------------------------------------------- our arm
 
 class Workload:
-    def __init__(self, B: int, T: int | None = None):
+    def __init__(self, B: int, T: int | None = None, kda: bool = False):
         """The Qwen3-Next-shaped layer at B rows; T = 1 is plain decode (a window
-        of one token through the same calls, checkpoint, ring and cursors)."""
+        of one token through the same calls, checkpoint, ring and cursors); kda:
+        one gate per key channel (the KDA variant) on the same shape."""
         from gated_delta_rule_spec_gb300 import inputs as gen
         c = gen.WORKLOADS["C2"]
         T = c.T if T is None else T
-        self.name = f"qwen3next-gdn-{'decode' if T == 1 else 'verify'}-b{B}" + (
+        self.kda = kda
+        self.name = f"qwen3next-{'kda' if kda else 'gdn'}-{'decode' if T == 1 else 'verify'}-b{B}" + (
             f"-t{T}" if T not in (1, c.T) else "")
         self.B, self.H, self.HV, self.K, self.V, self.T, self.L = B, c.H, c.HV, c.K, c.V, T, c.L
         self.num_slots = max(c.num_slots, B)
@@ -198,15 +200,16 @@ def build_state(wl: Workload, seed: int, device, random_rounds: int = 48):
     from gated_delta_rule_spec_gb300 import inputs as gen
 
     rng = gen.rng_for(seed, "bench", wl.B)
-    layer = binding.SpecLayer(wl.H, wl.HV, wl.K, wl.V, wl.T, wl.L, wl.num_slots, device=device)
+    layer = binding.SpecLayer(wl.H, wl.HV, wl.K, wl.V, wl.T, wl.L, wl.num_slots, per_key_gate=wl.kda,
+                              device=device)
     cur = binding.SpecCursors(wl.num_slots, device=device)
-    A_log, dt_bias = gen.layer_params(rng, wl.HV, wl.K, False)
+    A_log, dt_bias = gen.layer_params(rng, wl.HV, wl.K, wl.kda)
     A_log = torch.from_numpy(A_log).to(device)
     dt_bias = torch.from_numpy(dt_bias).to(device)
     slots = torch.from_numpy(gen.scattered_slots(rng, wl.num_slots, wl.B)).to(device)
 
     def dev_window():
-        w = gen.window_inputs(rng, wl.B, wl.T, wl.H, wl.HV, wl.K, wl.V, gen.BF16)
+        w = gen.window_inputs(rng, wl.B, wl.T, wl.H, wl.HV, wl.K, wl.V, gen.BF16, wl.kda)
         return {n: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
                 for n, x in w.items()}
 
@@ -232,7 +235,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     binding.load()
-    wl = Workload(args.batch, args.window)
+    wl = Workload(args.batch, args.window, args.kda)
     rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 1000 + rank, device,
                                                                      args.setup_rounds)
     path = binding.verify_path(layer)
@@ -329,7 +332,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     if args.steps // R > 0 and ev is not None:   # the verifies the events bracketed
         W_last = W_last[ev_steps]
     bytes_per_launch = float(np.mean([
-        verify_bytes_per_unit(Wr, wl.K, wl.V, wl.T, wl.G, wl.e, False).sum() * wl.HV
+        verify_bytes_per_unit(Wr, wl.K, wl.V, wl.T, wl.G, wl.e, wl.kda).sum() * wl.HV
         for Wr in W_last]))
     mean_W = float(W_last.mean())
 
@@ -483,7 +486,7 @@ def verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias, 
     return [statistics.median(times)]
 
 
-def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None) -> dict:
+def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None, kda: bool = False) -> dict:
     """The fp64 oracle, as it stands, on the host cores: verify of a sample of
     the workload's rows (all heads), ring fill W ~ U[0, L-2T] as in the sweep."""
     import oracle
@@ -494,17 +497,17 @@ def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None) -> dict:
         c = dataclasses.replace(c, T=T)
     rows = min(B, 16)
     rng = gen.rng_for(7, "cpu-baseline", rows)
-    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
-    ring = gen.garbage_ring(rng, rows, c.H, c.HV, c.L, c.K, c.V, gen.BF16)
+    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows, per_key_gate=kda)
+    ring = gen.garbage_ring(rng, rows, c.H, c.HV, c.L, c.K, c.V, gen.BF16, kda)
     ly = oracle.Layer(d, checkpoint=rng.standard_normal((rows, c.HV, c.V, c.K)) * 0.1,
                       rawv=gen.to_f64(ring["rawv"]), rawk=gen.to_f64(ring["rawk"]),
                       ring_g=-np.abs(ring["g"].astype(np.float64)),
                       ring_beta=np.abs(ring["beta"].astype(np.float64)) % 1.0)
     wp, base, flag = gen.random_cursors(rng, rows, c.L, c.T)
     cur = oracle.Cursors(rows, wp, base, flag)
-    A_log, dt = gen.layer_params(rng, c.HV, c.K, False)
+    A_log, dt = gen.layer_params(rng, c.HV, c.K, kda)
     w = {n: gen.to_f64(x) for n, x in
-         gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16).items()}
+         gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16, kda).items()}
     cores = os.cpu_count() or 1
     slot_idx = np.arange(rows, dtype=np.int32)
     reps, t0 = 0, time.perf_counter()
@@ -686,23 +689,23 @@ def run_reference(args, rank: int, world: int) -> dict | None:
     import oracle
     from gated_delta_rule_spec_gb300 import inputs as gen
 
-    wl = Workload(args.batch, args.window)
+    wl = Workload(args.batch, args.window, args.kda)
     c = dataclasses.replace(gen.WORKLOADS["C2"], T=wl.T)
     rows = 2
     rng = gen.rng_for(11, "reference-arm", rows)
-    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows)
-    ring = gen.garbage_ring(rng, rows, c.H, c.HV, c.L, c.K, c.V, gen.BF16)
+    d = oracle.Dims(H=c.H, HV=c.HV, K=c.K, V=c.V, T=c.T, L=c.L, num_slots=rows, per_key_gate=wl.kda)
+    ring = gen.garbage_ring(rng, rows, c.H, c.HV, c.L, c.K, c.V, gen.BF16, wl.kda)
     ly = oracle.Layer(d, checkpoint=rng.standard_normal((rows, c.HV, c.V, c.K)) * 0.1,
                       rawv=gen.to_f64(ring["rawv"]), rawk=gen.to_f64(ring["rawk"]),
                       ring_g=-np.abs(ring["g"].astype(np.float64)),
                       ring_beta=np.abs(ring["beta"].astype(np.float64)) % 1.0)
     wp, base, flag = gen.random_cursors(rng, rows, c.L, c.T)
     cur = oracle.Cursors(rows, wp, base, flag)
-    A_log, dt = gen.layer_params(rng, c.HV, c.K, False)
+    A_log, dt = gen.layer_params(rng, c.HV, c.K, wl.kda)
     slot_idx = np.arange(rows, dtype=np.int32)
     cores = os.cpu_count() or 1
     wins = [{n: gen.to_f64(x) for n, x in
-             gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16).items()}
+             gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16, wl.kda).items()}
             for _ in range(4)]
     accs = [gen.accept_lens(rng, rows, c.T) for _ in range(4)]
 
@@ -745,6 +748,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--window", type=int, default=None,
                     help="draft window T (default: the workload's 4; 1 = plain decode)")
+    ap.add_argument("--kda", action="store_true",
+                    help="the KDA variant (one gate per key channel) on the same shape")
     ap.add_argument("--prefill", type=int, default=0, metavar="N",
                     help="measure gdn_spec_prefill of --batch prompts of N tokens instead")
     ap.add_argument("--setup-rounds", type=int, default=48,
@@ -782,7 +787,7 @@ def main():
     else:
         line = run_ours(args, rank, world)
         if line is not None and world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args.batch, T=args.window)
+            line["cpu_baseline"] = cpu_baseline(args.batch, T=args.window, kda=args.kda)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
