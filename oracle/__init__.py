@@ -111,6 +111,10 @@ def _load(path: str | None = None):
         _lib.orc_prefill.restype = ctypes.c_uint32
         _lib.orc_prefill.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int] + [P] * 8 + [
             ctypes.c_int, ctypes.c_int]
+        _lib.orc_snapshot_verify.restype = ctypes.c_uint32
+        _lib.orc_snapshot_verify.argtypes = [P, P, P, ctypes.c_int] + [P] * 9
+        _lib.orc_snapshot_commit.restype = ctypes.c_uint32
+        _lib.orc_snapshot_commit.argtypes = [P, P, P, ctypes.c_int, P, P]
         _lib.orc_run.restype = None
         _lib.orc_run.argtypes = [P, P, ctypes.c_int, P, P, P, P]
         _lib.orc_run_batch.restype = None
@@ -341,6 +345,32 @@ def prefill(dims: Dims, layer: Layer, cursors: Cursors, slot_idx, q, k, v, a, b,
                              B, N, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
                              _ptr(dt_bias), _ptr(out), int(bool(from_zero)), int(nthreads))
     return out, int(st)
+
+
+def snapshot_verify(dims: Dims, layer: Layer, slot_idx, q, k, v, a, b, A_log, dt_bias):
+    """Comparison variant (the per-draft snapshot design the ring replaces):
+    returns (out [B,T,HV,V], snapshots [B,T,HV,V,K], status bits); the state
+    after each window token is stored, the checkpoint is only read."""
+    slot_idx = _i32(slot_idx)
+    B = slot_idx.shape[0]
+    q, k, v, a, b = _f64(q), _f64(k), _f64(v), _f64(a), _f64(b)
+    A_log, dt_bias = _f64(A_log), _f64(dt_bias)
+    out = np.zeros((B, dims.T, dims.HV, dims.V), np.float64)
+    snap = np.zeros((B, dims.T, dims.HV, dims.V, dims.K), np.float64)
+    cd, cl = dims._c(), layer._c()
+    st = _load().orc_snapshot_verify(ctypes.byref(cd), ctypes.byref(cl), _ptr(slot_idx), B, _ptr(q),
+                                     _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                     _ptr(out), _ptr(snap))
+    return out, snap, int(st)
+
+
+def snapshot_commit(dims: Dims, layer: Layer, slot_idx, accept_len, snap) -> int:
+    """Comparison variant: checkpoint[slot] = snap[b, accept_len - 1]."""
+    slot_idx, accept_len = _i32(slot_idx), _i32(accept_len)
+    snap = _f64(snap)
+    cd, cl = dims._c(), layer._c()
+    return int(_load().orc_snapshot_commit(ctypes.byref(cd), ctypes.byref(cl), _ptr(slot_idx),
+                                           slot_idx.shape[0], _ptr(accept_len), _ptr(snap)))
 
 
 def reset(dims: Dims, cursors: Cursors, slot_idx) -> int:

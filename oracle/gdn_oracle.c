@@ -626,3 +626,78 @@ uint32_t orc_prefill(const orc_dims *d, orc_layer *ly, orc_cursors *cur, const i
     }
     return st;
 }
+
+/* ------------------------------------------------------------------ */
+/* Comparison variant: the per-draft snapshot design that the ring       */
+/* replaces ([blog] §0-§1: the intermediate_ssm buffer, one full state   */
+/* per draft position).  Verify advances each row's state through the    */
+/* window, reads out every position and stores every intermediate state; */
+/* commit copies the state after the accepted tokens back.               */
+/* ------------------------------------------------------------------ */
+
+/* snap: [B, T, HV, V, K]; q, k: [B, T, H, K]; v: [B, T, HV, V]; a, b: [B, T, HV]
+ * (per-key gate: a [B, T, HV, K]); out: [B, T, HV, V].  Rows with slot < 0 or
+ * slot >= num_slots read out zeros and store nothing (status SLOT_OOR for
+ * the latter).  The checkpoint is only read. */
+uint32_t orc_snapshot_verify(const orc_dims *d, const orc_layer *ly, const int32_t *slot_idx, int B,
+                             const double *q, const double *k, const double *v, const double *a,
+                             const double *b, const double *A_log, const double *dt_bias,
+                             double *out, double *snap)
+{
+    const int K = d->K, V = d->V, T = d->T, H = d->H, HV = d->HV;
+    const size_t gw = g_width(d), VK = (size_t)V * K;
+    uint32_t st = 0;
+    double *S = (double *)malloc(sizeof(double) * VK);
+    double *g = (double *)malloc(sizeof(double) * gw);
+    for (int bb = 0; bb < B; ++bb) {
+        int slot = slot_idx[bb];
+        for (int hv = 0; hv < HV; ++hv) {
+            const int h = hv / (HV / H);
+            if (slot < 0 || slot >= d->num_slots) {
+                if (slot >= d->num_slots) st |= ORC_ST_SLOT_OOR;
+                for (int s = 0; s < T; ++s)
+                    memset(out + (((size_t)bb * T + s) * HV + hv) * V, 0, sizeof(double) * V);
+                continue;
+            }
+            memcpy(S, ly->checkpoint + ((size_t)slot * HV + hv) * VK, sizeof(double) * VK);
+            for (int s = 0; s < T; ++s) {
+                size_t tok = (size_t)bb * T + s;
+                if (d->per_key_gate) {
+                    for (int j = 0; j < K; ++j)
+                        g[j] = orc_gate_g(A_log[hv], a[(tok * HV + hv) * K + j], dt_bias[(size_t)hv * K + j]);
+                } else {
+                    g[0] = orc_gate_g(A_log[hv], a[tok * HV + hv], dt_bias[hv]);
+                }
+                orc_step(V, K, d->per_key_gate, S, v + (tok * HV + hv) * V, k + (tok * H + h) * K, g,
+                         orc_gate_beta(b[tok * HV + hv]), d->l2_eps);
+                orc_readout(V, K, S, q + (tok * H + h) * K, d->l2_eps, d->scale, out + (tok * HV + hv) * V);
+                memcpy(snap + (tok * HV + hv) * VK, S, sizeof(double) * VK);
+            }
+        }
+    }
+    free(g);
+    free(S);
+    return st;
+}
+
+/* checkpoint[slot] = snap[b, accept_len - 1] for rows with 1 <= accept_len <= T
+ * (accept_len 0 keeps the state; outside [0, T]: status ACCEPT_RANGE). */
+uint32_t orc_snapshot_commit(const orc_dims *d, orc_layer *ly, const int32_t *slot_idx, int B,
+                             const int32_t *accept_len, const double *snap)
+{
+    const int T = d->T, HV = d->HV;
+    const size_t VK = (size_t)d->V * d->K;
+    uint32_t st = 0;
+    for (int bb = 0; bb < B; ++bb) {
+        int slot = slot_idx[bb];
+        if (slot < 0) continue;
+        if (slot >= d->num_slots) { st |= ORC_ST_SLOT_OOR; continue; }
+        int acc = accept_len[bb];
+        if (acc < 0 || acc > T) { st |= ORC_ST_ACCEPT_RANGE; continue; }
+        if (acc == 0) continue;
+        for (int hv = 0; hv < HV; ++hv)
+            memcpy(ly->checkpoint + ((size_t)slot * HV + hv) * VK,
+                   snap + (((size_t)bb * T + acc - 1) * HV + hv) * VK, sizeof(double) * VK);
+    }
+    return st;
+}
