@@ -524,6 +524,111 @@ def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None, kda: bool 
                       f"{reps} repetitions in {el:.1f} s, W ~ U[0, {c.L - 2 * c.T}]"}
 
 
+# ----------------------------------------------------------------- snapshot comparison
+
+def snapshot_bytes_per_unit(K: int, V: int, T: int, G: int, e: int) -> float:
+    """Algorithmic bytes per (row, v-head) of one snapshot step: the state read,
+    T full states written, the window's q, k (shared by G v-heads), v, a, b
+    read, the outputs written, and the commit's copy of one state."""
+    return V * K * 4 + T * V * K * 4 + T * (2 * K * e / G + V * e + 2 * e) + T * V * e + 2 * V * K * 4
+
+
+def run_snapshot(args, rank: int, world: int) -> dict | None:
+    """The per-draft snapshot design (comparison variant) on the bench's
+    workload: a step is snapshot verify (T full states stored) + commit (the
+    accepted state copied back), captured in CUDA graphs."""
+    import torch
+    from gated_delta_rule_spec_gb300 import binding
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    wl = Workload(args.batch, args.window)
+    rng = gen.rng_for(4000 + rank, "snapshot", wl.B)
+    layer = binding.SpecLayer(wl.H, wl.HV, wl.K, wl.V, wl.T, wl.L, wl.num_slots, device=device)
+    layer.checkpoint.normal_(0.0, 0.1)
+    cur = binding.SpecCursors(wl.num_slots, device=device)
+    A_log, dt_bias = (torch.from_numpy(x).to(device) for x in gen.layer_params(rng, wl.HV, wl.K, False))
+    slots = torch.from_numpy(gen.scattered_slots(rng, wl.num_slots, wl.B)).to(device)
+    NI = 8
+    inputs = [{n: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device) for n, x in
+               gen.window_inputs(rng, wl.B, wl.T, wl.H, wl.HV, wl.K, wl.V, gen.BF16).items()}
+              for _ in range(NI)]
+    accs = [torch.from_numpy(gen.accept_lens(rng, wl.B, wl.T)).to(device) for _ in range(NI)]
+    out = torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device)
+    snap = torch.empty(wl.B, wl.T, wl.HV, wl.V, wl.K, dtype=torch.float32, device=device)
+
+    def step(i):
+        w = inputs[i % NI]
+        binding.snapshot_verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log,
+                                dt_bias, out=out, snap=snap)
+        binding.snapshot_commit(layer, cur, slots, accs[i % NI], snap)
+
+    for i in range(args.warmup):
+        step(i)
+    R = max(1, min(args.steps, 50))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(R):
+                step(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    reps = max(1, (args.steps + R - 1) // R)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    status = binding.read_status(cur)
+    if world > 1:
+        ms, = reduce_max([ms], device)
+    if rank != 0:
+        return None
+    steps = reps * R
+    t_step = ms / 1e3 / steps
+    peaks, peak_kind = measured_peaks()
+    byts = snapshot_bytes_per_unit(wl.K, wl.V, wl.T, wl.G, wl.e) * wl.B * wl.HV
+    achieved = byts / t_step / 1e9
+    return {
+        "metric": METRIC, "variant": "snapshot (comparison: per-draft full states, no ring)",
+        "value": round(world * wl.B * wl.T / t_step, 1), "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms / steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
+        "config": wl.config({"workload": wl.name.replace("-verify-", "-snapshot-verify-"),
+                             "step": "snapshot verify + snapshot commit",
+                             "snapshot_bytes": int(snap.numel() * 4)}),
+        "gpu_launches": 2 * steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "algorithmic_bytes_per_step": round(byts), "kernel": "snapshot verify + commit",
+                     "peak_kind": peak_kind},
+        # per (row, v-head, draft position): one full fp32 state; the ring path
+        # writes one raw record instead (V e + K e / G + 8 bytes)
+        "state_bytes_written_per_head_step": wl.V * wl.K * 4,
+        "ring_bytes_written_per_head_step": int(wl.V * wl.e + wl.K * wl.e / wl.G + 8),
+        "device_status": status,
+        "clocks": clocks,
+    }
+
 # ----------------------------------------------------------------- prefill
 
 PREFILL_METRIC = "prefilled tokens/s per GDN layer, 1\u00d7GB300"
@@ -750,6 +855,8 @@ def main():
                     help="draft window T (default: the workload's 4; 1 = plain decode)")
     ap.add_argument("--kda", action="store_true",
                     help="the KDA variant (one gate per key channel) on the same shape")
+    ap.add_argument("--variant", choices=("ring", "snapshot"), default="ring",
+                    help="snapshot: the per-draft state design the ring replaces (comparison)")
     ap.add_argument("--prefill", type=int, default=0, metavar="N",
                     help="measure gdn_spec_prefill of --batch prompts of N tokens instead")
     ap.add_argument("--setup-rounds", type=int, default=48,
@@ -778,6 +885,8 @@ def main():
                     "cpu_baseline": cb,
                     "e2e": {"value": cb["value"], "unit": cb["unit"], "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}
+    elif args.variant == "snapshot" and args.impl != "reference":
+        line = run_snapshot(args, rank, world)
     elif args.prefill:
         line = run_prefill(args, rank, world)
         if line is not None and world == 1 and not args.no_cpu_baseline:

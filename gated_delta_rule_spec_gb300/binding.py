@@ -50,6 +50,7 @@ class CursorDesc(ctypes.Structure):
 
 _lib = None
 EXPORTS = ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset", "gdn_spec_prefill",
+           "gdn_spec_snapshot_verify", "gdn_spec_snapshot_commit",
            "gdn_spec_read_status", "gdn_spec_strerror", "gdn_spec_abi_version",
            "gdn_spec_verify_path")
 
@@ -76,9 +77,12 @@ def load() -> ctypes.CDLL:
     lib.gdn_spec_fold.argtypes = [LP, I32, CP, P, I32, P]
     lib.gdn_spec_reset.argtypes = [CP, P, I32, P]
     lib.gdn_spec_prefill.argtypes = [LP, CP, P, I32, I32, P, P, P, P, P, P, P, P, I32, P]
+    lib.gdn_spec_snapshot_verify.argtypes = [LP, CP, P, I32, P, P, P, P, P, P, P, P, P, P]
+    lib.gdn_spec_snapshot_commit.argtypes = [LP, CP, P, I32, P, P, P]
     lib.gdn_spec_read_status.argtypes = [CP, ctypes.POINTER(ctypes.c_uint32), I32, P]
     for name in ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset",
-                 "gdn_spec_prefill", "gdn_spec_read_status"):
+                 "gdn_spec_prefill", "gdn_spec_snapshot_verify", "gdn_spec_snapshot_commit",
+                 "gdn_spec_read_status"):
         getattr(lib, name).restype = ctypes.c_int
     lib.gdn_spec_strerror.argtypes = [ctypes.c_int]
     lib.gdn_spec_strerror.restype = ctypes.c_char_p
@@ -235,6 +239,47 @@ def prefill(layer: SpecLayer, cursors: SpecCursors, slot_idx: torch.Tensor, q, k
                                  _stream(stream))
     _check(rc, "gdn_spec_prefill")
     return out
+
+
+def snapshot_verify(layer: SpecLayer, cursors: SpecCursors, slot_idx: torch.Tensor, q, k, v, a, b,
+                    A_log, dt_bias, out: torch.Tensor | None = None,
+                    snap: torch.Tensor | None = None, stream=None):
+    """Comparison variant (per-draft snapshots): returns (out [B, T, HV, V],
+    snap fp32 [B, T, HV, V, K]); the checkpoint is only read."""
+    B = slot_idx.shape[0]
+    shp = layer.window_shapes(B)
+    io = layer.io_torch
+    _need(slot_idx, "slot_idx", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need(t, name, io, shp[name])
+    _need(A_log, "A_log", torch.float32, shp["A_log"])
+    _need(dt_bias, "dt_bias", torch.float32, shp["dt_bias"])
+    if out is None:
+        out = torch.empty(shp["out"], dtype=io, device=q.device)
+    _need(out, "out", io, shp["out"])
+    sshape = (B, layer.T, layer.HV, layer.V, layer.K)
+    if snap is None:
+        snap = torch.empty(sshape, dtype=torch.float32, device=q.device)
+    _need(snap, "snap", torch.float32, sshape)
+    rc = load().gdn_spec_snapshot_verify(ctypes.byref(layer.desc()), ctypes.byref(cursors.desc()),
+                                         _ptr(slot_idx), B, _ptr(q), _ptr(k), _ptr(v), _ptr(a),
+                                         _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(out), _ptr(snap),
+                                         _stream(stream))
+    _check(rc, "gdn_spec_snapshot_verify")
+    return out, snap
+
+
+def snapshot_commit(layer: SpecLayer, cursors: SpecCursors, slot_idx: torch.Tensor,
+                    accept_len: torch.Tensor, snap: torch.Tensor, stream=None) -> None:
+    """Comparison variant: checkpoint[slot] = snap[b, accept_len - 1]."""
+    B = slot_idx.shape[0]
+    _need(slot_idx, "slot_idx", torch.int32, (B,))
+    _need(accept_len, "accept_len", torch.int32, (B,))
+    _need(snap, "snap", torch.float32, (B, layer.T, layer.HV, layer.V, layer.K))
+    rc = load().gdn_spec_snapshot_commit(ctypes.byref(layer.desc()), ctypes.byref(cursors.desc()),
+                                         _ptr(slot_idx), B, _ptr(accept_len), _ptr(snap),
+                                         _stream(stream))
+    _check(rc, "gdn_spec_snapshot_commit")
 
 
 def reset(cursors: SpecCursors, slot_idx: torch.Tensor, stream=None) -> None:

@@ -33,6 +33,13 @@ cudaError_t launch_prefill(const LayerArgs &P, const CursorArgs &C, bool kda, bo
                            const void *v, const void *a, const void *b, const float *A_log,
                            const float *dt_bias, void *out, int from_zero, cudaStream_t stream);
 size_t prefill_smem_bytes(int K, bool kda, bool bf16);
+cudaError_t launch_snapshot_verify(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
+                                   const int32_t *slot_idx, int B, const void *q, const void *k,
+                                   const void *v, const void *a, const void *b, const float *A_log,
+                                   const float *dt_bias, void *out, float *snap, cudaStream_t stream);
+cudaError_t launch_snapshot_commit(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
+                                   int B, const int32_t *accept_len, const float *snap,
+                                   cudaStream_t stream);
 }  // namespace gdnspec
 
 using namespace gdnspec;
@@ -221,6 +228,43 @@ int gdn_spec_prefill(const gdn_spec_layer *layer, const gdn_spec_cursors *cursor
     return cuda_rc(launch_prefill(layer_args(layer), cursor_args(cursors), kda, bf16, slot_idx, B, N,
                                   q, k, v, a, b, A_log, dt_bias, out, from_zero ? 1 : 0,
                                   static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_spec_snapshot_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
+                             const int32_t *slot_idx, int32_t B, const void *q, const void *k,
+                             const void *v, const void *a, const void *b, const float *A_log,
+                             const float *dt_bias, void *out, float *snap, void *stream) {
+    int rc = check_layer(layer);
+    if (rc) return rc;
+    if ((rc = check_cursors(cursors))) return rc;
+    if (cursors->num_slots != layer->num_slots) return GDN_SPEC_EINVAL;
+    if (B < 0) return GDN_SPEC_EINVAL;
+    if (B == 0) return GDN_SPEC_OK;
+    if (!slot_idx || !q || !k || !v || !a || !b || !A_log || !dt_bias || !out || !snap)
+        return GDN_SPEC_EINVAL;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(snap))
+        return GDN_SPEC_EALIGN;
+    const bool kda = layer->gate_kind == GDN_SPEC_GATE_PER_KEY;
+    const bool bf16 = layer->io_dtype == GDN_SPEC_DTYPE_BF16;
+    if (prefill_smem_bytes(layer->K, kda, bf16) > kMaxSmem) return GDN_SPEC_EUNSUPPORTED;
+    return cuda_rc(launch_snapshot_verify(layer_args(layer), cursor_args(cursors), kda, bf16, slot_idx, B,
+                                          q, k, v, a, b, A_log, dt_bias, out, snap,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_spec_snapshot_commit(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
+                             const int32_t *slot_idx, int32_t B, const int32_t *accept_len,
+                             const float *snap, void *stream) {
+    int rc = check_layer(layer);
+    if (rc) return rc;
+    if ((rc = check_cursors(cursors))) return rc;
+    if (cursors->num_slots != layer->num_slots) return GDN_SPEC_EINVAL;
+    if (B < 0) return GDN_SPEC_EINVAL;
+    if (B == 0) return GDN_SPEC_OK;
+    if (!slot_idx || !accept_len || !snap) return GDN_SPEC_EINVAL;
+    if (!aligned16(snap)) return GDN_SPEC_EALIGN;
+    return cuda_rc(launch_snapshot_commit(layer_args(layer), cursor_args(cursors), slot_idx, B,
+                                          accept_len, snap, static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_spec_reset(const gdn_spec_cursors *cursors, const int32_t *slot_idx, int32_t B,

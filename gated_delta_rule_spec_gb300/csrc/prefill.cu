@@ -18,6 +18,14 @@
 // The prompt streams through shared memory in chunks of 64 tokens, brought in
 // by 1-D bulk asynchronous copies on an mbarrier (one row per token for k, q
 // and the block's v values); the gates are computed from a and b meanwhile.
+//
+// The same kernel, instantiated with SNAP, is the comparison variant of the
+// per-draft snapshot design that the ReplaySSM ring replaces (blog §0-§1, the
+// intermediate_ssm buffer): it advances each row's state through the draft
+// window from the checkpoint, reads out every position and stores the full
+// state after every position (one V x K fp32 state per (row, position,
+// v-head)); the checkpoint is only read and no cursor is touched.  Its commit
+// copies the state after the accepted tokens back into the checkpoint.
 #include "common.cuh"
 #include "ptx_sm100.cuh"
 #include "replay.cuh"
@@ -65,12 +73,13 @@ __device__ __forceinline__ bool prefill_row_ok(const CursorArgs &C, int slot, in
 
 constexpr int kPreCtasPerSm = 3;   // registers: two state rows, a key or query chunk, sums
 
-template <typename IO, bool KDA, int K>
+template <typename IO, bool KDA, int K, bool SNAP>
 __global__ void __launch_bounds__(kPreThreads, kPreCtasPerSm)
 prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, int B, int N,
                const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                const IO *__restrict__ a, const IO *__restrict__ bgate, const float *__restrict__ A_log,
-               const float *__restrict__ dt_bias, IO *__restrict__ out, int from_zero) {
+               const float *__restrict__ dt_bias, IO *__restrict__ out, int from_zero,
+               float *__restrict__ snap) {
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
     constexpr int kPer = KC::kVals;                 // values per 16-byte chunk
@@ -108,8 +117,10 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
         const int row0 = vbk * kPreRows;
         const int nrows = V - row0 < kPreRows ? V - row0 : kPreRows;   // a multiple of 8
         const int slot = slot_idx[bb];
-        uint32_t st;
-        if (!prefill_row_ok(C, slot, L, from_zero, &st)) {
+        uint32_t st = 0;
+        const bool row_ok = SNAP ? (slot >= 0 && slot < C.num_slots) : prefill_row_ok(C, slot, L, from_zero, &st);
+        if (SNAP && slot >= C.num_slots) st = GDN_SPEC_ST_SLOT_OOR;
+        if (!row_ok) {
             if (st && hv == 0 && vbk == 0 && tid == 0) atomicOr(C.status, st);
             // a skipped row reads out zeros
             for (int idx = tid; idx < N * nrows; idx += kPreThreads) {
@@ -128,7 +139,7 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
         for (int rr = 0; rr < 2; ++rr) {
 #pragma unroll
             for (int i = 0; i < kNP; ++i) S[rr][i] = make_float2(0.f, 0.f);
-            if (!from_zero && (rr ? valid1 : valid0)) {
+            if ((SNAP || !from_zero) && (rr ? valid1 : valid0)) {
                 const float *srow = ckpt + (sh_hv * V + row0 + pair + rr * kPrePairs) * K;
 #pragma unroll
                 for (int m = 0; m < kNC; ++m) {
@@ -320,10 +331,31 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
                     if (valid0) out[o] = IO(f * w0);
                     if (valid1) out[o + kPrePairs] = IO(f * w1);
                 }
+                if (SNAP) {   // the full state after this position
+                    const float2 g2 = make_float2(gam, gam);
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        if (!(rr ? valid1 : valid0)) continue;
+                        float *drow = snap + ((((size_t)bb * N + c0 + t) * HV + hv) * V + row0 + pair +
+                                              rr * kPrePairs) * K;
+#pragma unroll
+                        for (int m = 0; m < kNC; ++m) {
+                            float4 *dst = reinterpret_cast<float4 *>(drow + (part + 4 * m) * kPer);
+#pragma unroll
+                            for (int qq = 0; qq < kPer / 4; ++qq) {
+                                const int i = m * (kPer / 2) + 2 * qq;
+                                const float2 x0 = KDA ? S[rr][i] : __fmul2_rn(S[rr][i], g2);
+                                const float2 x1 = KDA ? S[rr][i + 1] : __fmul2_rn(S[rr][i + 1], g2);
+                                dst[qq] = make_float4(x0.x, x0.y, x1.x, x1.y);
+                            }
+                        }
+                    }
+                }
             }
             __syncthreads();   // the chunk's buffers are reused by the next chunk
         }
         if (failed) return;
+        if (SNAP) continue;   // the snapshot variant only reads the checkpoint
 
         // ---- 5. S = gam R into the checkpoint
         const float2 g2 = make_float2(gam, gam);
@@ -359,17 +391,42 @@ __global__ void prefill_cursor_kernel(CursorArgs C, int L, const int32_t *__rest
     }
 }
 
-template <typename IO, bool KDA, int K>
+// checkpoint[slot, hv] = snap[b, accept_len - 1, hv] for 1 <= accept_len <= T
+// (0 keeps the state); one CTA per (row, v-head), 16-byte copies
+__global__ void snapshot_commit_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx,
+                                       int B, const int32_t *__restrict__ accept_len,
+                                       const float *__restrict__ snap) {
+    const int bb = blockIdx.x / P.HV, hv = blockIdx.x % P.HV;
+    const int slot = slot_idx[bb];
+    if (slot < 0) return;
+    if (slot >= C.num_slots) {
+        if (hv == 0 && threadIdx.x == 0) atomicOr(C.status, GDN_SPEC_ST_SLOT_OOR);
+        return;
+    }
+    const int acc = accept_len[bb];
+    if (acc < 0 || acc > P.T) {
+        if (hv == 0 && threadIdx.x == 0) atomicOr(C.status, GDN_SPEC_ST_ACCEPT_RANGE);
+        return;
+    }
+    if (acc == 0) return;
+    const size_t n4 = (size_t)P.V * P.K / 4;
+    const float4 *src = reinterpret_cast<const float4 *>(snap + (((size_t)bb * P.T + acc - 1) * P.HV + hv) * P.V * P.K);
+    float4 *dst = reinterpret_cast<float4 *>(P.checkpoint + ((size_t)slot * P.HV + hv) * P.V * P.K);
+    for (size_t i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+}
+
+template <typename IO, bool KDA, int K, bool SNAP>
 static cudaError_t launch_prefill_k(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
                                     int B, int N, const void *q, const void *k, const void *v,
                                     const void *a, const void *b, const float *A_log,
-                                    const float *dt_bias, void *out, int from_zero, cudaStream_t stream) {
+                                    const float *dt_bias, void *out, int from_zero, float *snap,
+                                    cudaStream_t stream) {
     const size_t smem = PrefillSmem(K, KDA, sizeof(IO)).total;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    auto kern = prefill_kernel<IO, KDA, K>;
+    auto kern = prefill_kernel<IO, KDA, K, SNAP>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const long long items = (long long)B * P.HV * ((P.V + kPreRows - 1) / kPreRows);
@@ -379,37 +436,63 @@ static cudaError_t launch_prefill_k(const LayerArgs &P, const CursorArgs &C, con
         kern<<<grid, kPreThreads, smem, stream>>>(
             P, C, slot_idx, B, N, static_cast<const IO *>(q), static_cast<const IO *>(k),
             static_cast<const IO *>(v), static_cast<const IO *>(a), static_cast<const IO *>(b), A_log,
-            dt_bias, static_cast<IO *>(out), from_zero);
+            dt_bias, static_cast<IO *>(out), from_zero, snap);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (SNAP) return cudaSuccess;
     const int cb = (B + 255) / 256;
     prefill_cursor_kernel<<<cb < 1 ? 1 : (cb > 64 ? 64 : cb), 256, 0, stream>>>(C, P.L, slot_idx, B,
                                                                                  from_zero);
     return cudaGetLastError();
 }
 
-template <typename IO, bool KDA>
+template <typename IO, bool KDA, bool SNAP>
 static cudaError_t launch_prefill_typed(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
                                         int B, int N, const void *q, const void *k, const void *v,
                                         const void *a, const void *b, const float *A_log,
-                                        const float *dt_bias, void *out, int from_zero,
+                                        const float *dt_bias, void *out, int from_zero, float *snap,
                                         cudaStream_t stream) {
     switch (P.K) {
-        case 32: return launch_prefill_k<IO, KDA, 32>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream);
-        case 64: return launch_prefill_k<IO, KDA, 64>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream);
-        case 128: return launch_prefill_k<IO, KDA, 128>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream);
+        case 32: return launch_prefill_k<IO, KDA, 32, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream);
+        case 64: return launch_prefill_k<IO, KDA, 64, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream);
+        case 128: return launch_prefill_k<IO, KDA, 128, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <bool SNAP>
+static cudaError_t launch_any(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
+                              const int32_t *slot_idx, int B, int N, const void *q, const void *k,
+                              const void *v, const void *a, const void *b, const float *A_log,
+                              const float *dt_bias, void *out, int from_zero, float *snap,
+                              cudaStream_t stream) {
+    if (bf16)
+        return kda ? launch_prefill_typed<__nv_bfloat16, true, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream)
+                   : launch_prefill_typed<__nv_bfloat16, false, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream);
+    return kda ? launch_prefill_typed<float, true, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream)
+               : launch_prefill_typed<float, false, SNAP>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, snap, stream);
 }
 
 cudaError_t launch_prefill(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
                            const int32_t *slot_idx, int B, int N, const void *q, const void *k,
                            const void *v, const void *a, const void *b, const float *A_log,
                            const float *dt_bias, void *out, int from_zero, cudaStream_t stream) {
-    if (bf16)
-        return kda ? launch_prefill_typed<__nv_bfloat16, true>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream)
-                   : launch_prefill_typed<__nv_bfloat16, false>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream);
-    return kda ? launch_prefill_typed<float, true>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream)
-               : launch_prefill_typed<float, false>(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out, from_zero, stream);
+    return launch_any<false>(P, C, kda, bf16, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out,
+                             from_zero, nullptr, stream);
+}
+
+cudaError_t launch_snapshot_verify(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
+                                   const int32_t *slot_idx, int B, const void *q, const void *k,
+                                   const void *v, const void *a, const void *b, const float *A_log,
+                                   const float *dt_bias, void *out, float *snap, cudaStream_t stream) {
+    return launch_any<true>(P, C, kda, bf16, slot_idx, B, P.T, q, k, v, a, b, A_log, dt_bias, out, 0,
+                            snap, stream);
+}
+
+cudaError_t launch_snapshot_commit(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
+                                   int B, const int32_t *accept_len, const float *snap,
+                                   cudaStream_t stream) {
+    snapshot_commit_kernel<<<B * P.HV, 256, 0, stream>>>(P, C, slot_idx, B, accept_len, snap);
+    return cudaGetLastError();
 }
 
 }  // namespace gdnspec

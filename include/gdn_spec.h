@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define GDN_SPEC_ABI_VERSION 2   /* 2: adds gdn_spec_prefill */
+#define GDN_SPEC_ABI_VERSION 2   /* 2: adds gdn_spec_prefill and the snapshot comparison calls */
 
 /* host-side error codes (return values) */
 #define GDN_SPEC_OK            0
@@ -211,6 +211,34 @@ int gdn_spec_prefill(const gdn_spec_layer *layer, const gdn_spec_cursors *cursor
                      const void *q, const void *k, const void *v, const void *a,
                      const void *b, const float *A_log, const float *dt_bias, void *out,
                      int32_t from_zero, void *stream);
+
+/*
+ * Comparison variant, not part of the ring path: the per-draft snapshot
+ * design that the ReplaySSM ring replaces ([blog] §0-§1: the intermediate_ssm
+ * buffer, one full state per draft position), kept so that its cost can be
+ * measured beside the ring on the same machine.
+ *
+ * gdn_spec_snapshot_verify -- for every row and v-head, from the slot's
+ * checkpoint, advance through the T window tokens, write every position's
+ * output and store the full state after every position:
+ *   snap      fp32 [B, T, HV, V, K]  (written; caller-owned; T V K 4 bytes
+ *             per (row, v-head): 256 KiB at the Qwen3-Next shape and T = 4)
+ *   q, k, v, a, b, A_log, dt_bias, out: as gdn_spec_verify.
+ * The checkpoint is only read; cursors and ring are not used (the status
+ * word records SLOT_OOR).
+ *
+ * gdn_spec_snapshot_commit -- checkpoint[slot_idx[b]] = snap[b, accept_len[b]
+ * - 1] for 1 <= accept_len <= T (0 keeps the state; outside [0, T]:
+ * ACCEPT_RANGE); accept_len int32 [B], device.
+ */
+int gdn_spec_snapshot_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
+                             const int32_t *slot_idx, int32_t B,
+                             const void *q, const void *k, const void *v, const void *a,
+                             const void *b, const float *A_log, const float *dt_bias, void *out,
+                             float *snap, void *stream);
+int gdn_spec_snapshot_commit(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
+                             const int32_t *slot_idx, int32_t B, const int32_t *accept_len,
+                             const float *snap, void *stream);
 
 /*
  * gdn_spec_read_status -- copy the device status word to *host_out after
