@@ -1,5 +1,5 @@
 // verify_generic.cu -- CUDA-core verify kernel for any supported shape
-// (fp32 or bf16 I/O, GDN or KDA gate, K <= 256, L <= 128).
+// (fp32 or bf16 I/O, GDN or KDA gate, K in {32, 64, 128}, L <= 128).
 //
 // One CTA per (V-block of 128 rows, batch row, v-head); no layer axis, since
 // layers are chain-dependent inside the forward (blog post on sglang PR
@@ -32,6 +32,7 @@
 // and beta computed here.  rawk is written by one CTA per k-head (hv % G == 0,
 // V-block 0), g and beta by V-block 0 (sglang PR #36821 ring-write placement).
 #include "common.cuh"
+#include "ptx_sm100.cuh"
 
 namespace gdnspec {
 
@@ -55,14 +56,16 @@ __host__ __device__ inline GenSmem gen_smem_layout(int K, int L, int T, bool kda
     s.T = T;
     s.K = K;
     s.kda = kda;
+    // every region starts on 16 bytes (a multiple of 4 floats): float4 reads
+    auto up4 = [](size_t x) { return (x + 3) & ~(size_t)3; };
     size_t off = 0;
-    s.x = off;     off += (size_t)(L + T) * s.KP;         // rows: n keys then T queries (n <= L)
-    s.alpha = off; off += (size_t)L * (kda ? K : 1);
-    s.beta = off;  off += (size_t)L;
-    s.A = off;     off += (size_t)L * (L + 1);
-    s.F = off;     off += (size_t)T * L;
-    s.c = off;     off += (size_t)T * L;
-    s.qeff = off;  off += (size_t)T * K;
+    s.x = off;     off = up4(off + (size_t)(L + T) * s.KP);   // rows: n keys then T queries (n <= L)
+    s.alpha = off; off = up4(off + (size_t)L * (kda ? K : 1));
+    s.beta = off;  off = up4(off + (size_t)L);
+    s.A = off;     off = up4(off + (size_t)L * (L + 1));
+    s.F = off;     off = up4(off + (size_t)T * L);
+    s.c = off;     off = up4(off + (size_t)T * L);
+    s.qeff = off;  off = up4(off + (size_t)T * K);
     s.total = off;
     return s;
 }
@@ -124,6 +127,16 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
     IO *rawk_w = reinterpret_cast<IO *>(P.rawk);
     IO *rawv_w = reinterpret_cast<IO *>(P.rawv);
     const bool k_writer = (hv % P.G == 0) && vb == 0;
+    if (tid == 0) {   // the checkpoint tile and the v history into L2 now; read at the end
+        const int rows = V - v0 < kGenThreads ? V - v0 : kGenThreads;
+        ptx::prefetch_l2(P.checkpoint + (sh_hv * V + v0) * K, (uint32_t)rows * K * 4);
+        if (V == kGenThreads) {   // whole records are contiguous: one or two segments
+            const int first = (L - base) < W ? (L - base) : W;
+            if (first > 0)
+                ptx::prefetch_l2(rawv + (sh_hv * L + base) * V, (uint32_t)(first * V * sizeof(IO)));
+            if (W > first) ptx::prefetch_l2(rawv + sh_hv * L * V, (uint32_t)((W - first) * V * sizeof(IO)));
+        }
+    }
 
     // ---- 1. keys (history + window) and window queries, L2-normalised into X
     for (int j = warp; j < n + T; j += kGenThreads / 32) {
@@ -198,63 +211,65 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
     for (int idx = tid; idx < T * L; idx += kGenThreads) Fm[idx] = 0.0f;
     __syncthreads();
 
-    // ---- 3. A and F: one warp per column r, decays as running products
+    // ---- 3. A and F: four threads per token row i (a quarter of K each)
+    //         walk r down from i - 1 with the decay Gamma(i, r) as a running
+    //         product; a window row i = W + s also forms F[s, r] against q^_s.
+    //         Rows are interleaved over the warps (the triangle stays
+    //         balanced) and every loop bound is the same in a warp, so the
+    //         two-level shuffles of the dot products are warp-wide.
     {
-        constexpr int KMAX = 256 / 32;
+        constexpr int KQ = 32;                 // channels per thread, K <= 128
+        const int part = tid & 3, grp = tid >> 2;
+        const int kq = K / 4, k0 = part * kq;
         const float *Q = X + (size_t)n * KP;
-        for (int r = warp; r < n; r += kGenThreads / 32) {
-            float xr[KMAX], cdec[KMAX];
+        for (int pass = 0; pass * 32 < n; ++pass) {
+            const int i = pass * 32 + (grp & 7) * 4 + warp;
+            const bool live = i < n, win = live && i >= W;
+            const int s = i - W;
+            float xi[KQ], xq[KQ], c[KQ];
 #pragma unroll
-            for (int m = 0; m < KMAX; ++m) {
-                const int kk = lane + 32 * m;
-                xr[m] = kk < K ? X[r * KP + kk] : 0.0f;
-                cdec[m] = 1.0f;
+            for (int m = 0; m < KQ; ++m) {
+                const bool in = m < kq;
+                xi[m] = (in && live) ? X[i * KP + k0 + m] : 0.0f;
+                xq[m] = (in && win) ? Q[s * KP + k0 + m] : 0.0f;
+                c[m] = 1.0f;
             }
-            float cs = 1.0f;  // GDN: scalar decay Gamma(i, r)
-            if (r >= W) {  // Gamma(r, r) = 1
-                const int s = r - W;
+            float cs = 1.0f;
+            {   // F[s, i] = <k^_i, q^_s> (Gamma = 1)
                 float acc = 0.0f;
 #pragma unroll
-                for (int m = 0; m < KMAX; ++m) {
-                    const int kk = lane + 32 * m;
-                    if (kk < K) acc += xr[m] * Q[s * KP + kk];
-                }
-                acc = warp_sum(acc);
-                if (lane == 0) Fm[s * L + r] = acc;
+                for (int m = 0; m < KQ; ++m) acc = fmaf(xi[m], xq[m], acc);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                if (win && part == 0) Fm[s * L + i] = acc;
             }
-            for (int i = r + 1; i < n; ++i) {
-                float acc = 0.0f, accq = 0.0f;
-                const bool win = i >= W;
-                const int s = i - W;
+            const float bi = live ? betaS[i] : 0.0f;
+            const int top = min(pass * 32 + 28 + warp, n - 1);   // largest row of this warp
+            for (int r = top - 1; r >= 0; --r) {
+                const bool act = live && r < i;
                 if (KDA) {
 #pragma unroll
-                    for (int m = 0; m < KMAX; ++m) {
-                        const int kk = lane + 32 * m;
-                        if (kk < K) {
-                            cdec[m] *= alpha[i * K + kk];
-                            const float w = xr[m] * cdec[m];
-                            acc += w * X[i * KP + kk];
-                            if (win) accq += w * Q[s * KP + kk];
-                        }
-                    }
-                } else {
-                    cs *= alpha[i];
-#pragma unroll
-                    for (int m = 0; m < KMAX; ++m) {
-                        const int kk = lane + 32 * m;
-                        if (kk < K) {
-                            acc += xr[m] * X[i * KP + kk];
-                            if (win) accq += xr[m] * Q[s * KP + kk];
-                        }
-                    }
-                    acc *= cs;
-                    accq *= cs;
+                    for (int m = 0; m < KQ; ++m)
+                        if (m < kq && act) c[m] *= alpha[(r + 1) * K + k0 + m];
+                } else if (act) {
+                    cs *= alpha[r + 1];
                 }
-                acc = warp_sum(acc);
-                if (win) accq = warp_sum(accq);
-                if (lane == 0) {
-                    Am[i * LA + r] = betaS[i] * acc;
-                    if (win) Fm[s * L + r] = accq;
+                float acc = 0.0f, accq = 0.0f;
+#pragma unroll
+                for (int m = 0; m < KQ; ++m) {
+                    if (m < kq) {
+                        const float w = c[m] * X[r * KP + k0 + m];
+                        acc = fmaf(xi[m], w, acc);
+                        accq = fmaf(xq[m], w, accq);
+                    }
+                }
+                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                accq += __shfl_xor_sync(0xffffffffu, accq, 1);
+                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                accq += __shfl_xor_sync(0xffffffffu, accq, 2);
+                if (act && part == 0) {
+                    Am[i * LA + r] = bi * acc * cs;
+                    if (win) Fm[s * L + r] = accq * cs;
                 }
             }
         }
@@ -288,32 +303,49 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
     }
     __syncthreads();
 
-    // ---- 6. o_s = scale (S0 q_eff_s + sum_j c[s, j] v_j) for this thread's row
+    // ---- 6. o_s = scale (S0 q_eff_s + sum_j c[s, j] v_j) for this thread's row;
+    //         global reads in batches of eight, so that a batch costs one round trip
     if (vrow < V) {
+        constexpr int kBatch = 8;
         float acc[kGenMaxT];
 #pragma unroll
         for (int s = 0; s < kGenMaxT; ++s) acc[s] = 0.0f;
         const float4 *srow =
             reinterpret_cast<const float4 *>(P.checkpoint + (sh_hv * V + vrow) * K);
-        for (int k4 = 0; k4 < K / 4; ++k4) {
-            const float4 sv = srow[k4];
+        for (int k4 = 0; k4 < K / 4; k4 += kBatch) {   // K / 4 is a multiple of 8
+            float4 sv[kBatch];
 #pragma unroll
-            for (int s = 0; s < kGenMaxT; ++s) {
-                if (s < T) {
-                    const float *qe = qeff + s * K + 4 * k4;
-                    acc[s] += sv.x * qe[0] + sv.y * qe[1] + sv.z * qe[2] + sv.w * qe[3];
+            for (int u = 0; u < kBatch; ++u) sv[u] = srow[k4 + u];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+#pragma unroll
+                for (int s = 0; s < kGenMaxT; ++s) {
+                    if (s < T) {
+                        const float4 qe = *reinterpret_cast<const float4 *>(qeff + s * K + 4 * (k4 + u));
+                        acc[s] += sv[u].x * qe.x + sv[u].y * qe.y + sv[u].z * qe.z + sv[u].w * qe.w;
+                    }
                 }
             }
         }
-        for (int j = 0; j < n; ++j) {
-            float vj;
-            if (j < W)
-                vj = to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vrow]);
-            else
-                vj = to_f32<IO>(v[(((size_t)bb * T + (j - W)) * HV + hv) * V + vrow]);
+        for (int j0 = 0; j0 < n; j0 += kBatch) {
+            float vj[kBatch];
 #pragma unroll
-            for (int s = 0; s < kGenMaxT; ++s)
-                if (s < T) acc[s] += cm[s * L + j] * vj;
+            for (int u = 0; u < kBatch; ++u) {
+                const int j = j0 + u;
+                vj[u] = 0.0f;
+                if (j < W)
+                    vj[u] = to_f32<IO>(rawv[(sh_hv * L + ring_pos(base, j, L)) * V + vrow]);
+                else if (j < n)
+                    vj[u] = to_f32<IO>(v[(((size_t)bb * T + (j - W)) * HV + hv) * V + vrow]);
+            }
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                if (j0 + u < n) {
+#pragma unroll
+                    for (int s = 0; s < kGenMaxT; ++s)
+                        if (s < T) acc[s] += cm[s * L + j0 + u] * vj[u];
+                }
+            }
         }
 #pragma unroll
         for (int s = 0; s < kGenMaxT; ++s)
