@@ -162,20 +162,35 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
         }
     }
     // ---- 2. gates: history from the ring, window computed (and written to the ring)
-    if (KDA) {
-        for (int idx = tid; idx < n * K; idx += kGenThreads) {
-            const int j = idx / K, kk = idx - j * K;
-            const int p = ring_pos(base, j, L);
-            float g;
-            if (j < W) {
-                g = P.ring_g[(sh_hv * L + p) * K + kk];
-            } else {
-                const size_t tok = (size_t)bb * T + (j - W);
-                g = gate_g(A_log[hv], to_f32<IO>(a[(tok * HV + hv) * K + kk]),
-                           dt_bias[(size_t)hv * K + kk]);
-                if (vb == 0) P.ring_g[(sh_hv * L + p) * K + kk] = g;
+    if (KDA) {   // n K gates: eight loads in flight per thread before any is used
+        constexpr int kB = 8;
+        for (int idx0 = tid; idx0 < n * K; idx0 += kB * kGenThreads) {
+            float raw[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int idx = idx0 + u * kGenThreads;
+                const int j = idx / K, kk = idx - j * K;
+                raw[u] = 0.0f;
+                if (idx < n * K) {
+                    if (j < W)
+                        raw[u] = P.ring_g[(sh_hv * L + ring_pos(base, j, L)) * K + kk];
+                    else
+                        raw[u] = to_f32<IO>(a[(((size_t)bb * T + (j - W)) * HV + hv) * K + kk]);
+                }
             }
-            alpha[j * K + kk] = expf(g);
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int idx = idx0 + u * kGenThreads;
+                if (idx < n * K) {
+                    const int j = idx / K, kk = idx - j * K;
+                    float g = raw[u];
+                    if (j >= W) {
+                        g = gate_g(A_log[hv], raw[u], dt_bias[(size_t)hv * K + kk]);
+                        if (vb == 0) P.ring_g[(sh_hv * L + ring_pos(base, j, L)) * K + kk] = g;
+                    }
+                    alpha[j * K + kk] = expf(g);
+                }
+            }
         }
     } else {
         for (int j = tid; j < n; j += kGenThreads) {
@@ -218,9 +233,13 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
     //         balanced) and every loop bound is the same in a warp, so the
     //         two-level shuffles of the dot products are warp-wide.
     {
+        // a thread owns the 16-byte chunks part, part + 4, part + 8, ... of a
+        // row (chunk c = channels 4c..4c+3): the four parts of a row read
+        // consecutive chunks, so their shared-memory reads share no bank
         constexpr int KQ = 32;                 // channels per thread, K <= 128
+        constexpr int KQ4 = KQ / 4;
         const int part = tid & 3, grp = tid >> 2;
-        const int kq = K / 4, k0 = part * kq;
+        const int kq4 = K / 16;                // chunks per thread
         const float *Q = X + (size_t)n * KP;
         for (int pass = 0; pass * 32 < n; ++pass) {
             const int i = pass * 32 + (grp & 7) * 4 + warp;
@@ -229,9 +248,10 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
             float xi[KQ], xq[KQ], c[KQ];
 #pragma unroll
             for (int m = 0; m < KQ; ++m) {
-                const bool in = m < kq;
-                xi[m] = (in && live) ? X[i * KP + k0 + m] : 0.0f;
-                xq[m] = (in && win) ? Q[s * KP + k0 + m] : 0.0f;
+                const bool in = (m >> 2) < kq4;
+                const int ch = 4 * (part + 4 * (m >> 2)) + (m & 3);
+                xi[m] = (in && live) ? X[i * KP + ch] : 0.0f;
+                xq[m] = (in && win) ? Q[s * KP + ch] : 0.0f;
                 c[m] = 1.0f;
             }
             float cs = 1.0f;
@@ -249,18 +269,30 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
                 const bool act = live && r < i;
                 if (KDA) {
 #pragma unroll
-                    for (int m = 0; m < KQ; ++m)
-                        if (m < kq && act) c[m] *= alpha[(r + 1) * K + k0 + m];
+                    for (int m4 = 0; m4 < KQ4; ++m4) {
+                        if (m4 < kq4) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(alpha + (r + 1) * K + 4 * (part + 4 * m4));
+                            c[4 * m4] *= act ? a4.x : 1.0f;
+                            c[4 * m4 + 1] *= act ? a4.y : 1.0f;
+                            c[4 * m4 + 2] *= act ? a4.z : 1.0f;
+                            c[4 * m4 + 3] *= act ? a4.w : 1.0f;
+                        }
+                    }
                 } else if (act) {
                     cs *= alpha[r + 1];
                 }
                 float acc = 0.0f, accq = 0.0f;
 #pragma unroll
-                for (int m = 0; m < KQ; ++m) {
-                    if (m < kq) {
-                        const float w = c[m] * X[r * KP + k0 + m];
-                        acc = fmaf(xi[m], w, acc);
-                        accq = fmaf(xq[m], w, accq);
+                for (int m4 = 0; m4 < KQ4; ++m4) {
+                    if (m4 < kq4) {
+                        const float4 x4 = *reinterpret_cast<const float4 *>(X + r * KP + 4 * (part + 4 * m4));
+                        const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float w = c[4 * m4 + e] * xs[e];
+                            acc = fmaf(xi[4 * m4 + e], w, acc);
+                            accq = fmaf(xq[4 * m4 + e], w, accq);
+                        }
                     }
                 }
                 acc += __shfl_xor_sync(0xffffffffu, acc, 1);
