@@ -72,12 +72,13 @@ def mirror_cursors(wp, base, acc_rows, T, L):
     return np.array(out)
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(path_name: str = "tc") -> str:
+    """Hash of the sources of one verify path (its kernel file and the headers
+    it includes), which keys the committed ncu traffic record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_spec_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.startswith("verify") or name in ("common.cuh", "ptx_sm100.cuh"):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in (f"verify_{path_name}.cu", "common.cuh", "ptx_sm100.cuh"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -91,7 +92,7 @@ def profiled_traffic(path_name: str, B: int, T: int):
         rec = json.load(open(f))
     except Exception:
         return None
-    if rec.get("kernel_source_hash") != kernel_source_hash() or rec.get("T") != T:
+    if rec.get("kernel_source_hash") != kernel_source_hash(path_name) or rec.get("T") != T:
         return None
     per_row = rec.get("dram_bytes_per_launch_per_row")
     return None if per_row is None else float(per_row) * B
