@@ -14,7 +14,7 @@
 //   per row i  A[i, r] = beta_i Gamma(i, r) G[i, r], F[i, s] = Gamma(W+s, i) G[i, 64+s]
 //              (one thread per token; decays are products of alpha, never
 //              exponentials of differences of long sums)
-//   M          M (I + A) = F^T, backward substitution, one warp for all T rows
+//   M          M (I + A) = F^T, backward substitution, one warp per window token
 //   q_eff_s    eG_{W+s} q^_s - sum_j M[s, j] beta_j eG_j k^_j       (K-vector)
 //   P          P = S0 q_eff^T: the checkpoint tile times T columns
 //              -> tcgen05.mma kind::tf32 with S0 staged by TMA.
