@@ -41,11 +41,12 @@ def test_reduce_max_over_two_gloo_ranks():
     assert res[0] == res[1] == [20.0, 0.0]
 
 
-def test_torchrun_two_ranks_prints_one_line():
-    port = 29700 + os.getpid() % 1000
+@pytest.mark.parametrize("extra", [[], ["--prefill", "32", "--batch", "2"]])
+def test_torchrun_two_ranks_prints_one_line(extra):
+    port = 29700 + os.getpid() % 1000 + (50 if extra else 0)
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr=127.0.0.1", f"--master-port={port}", os.path.join(ROOT, "bench.py"),
-           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3"]
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3"] + extra
     env = dict(os.environ, OMP_NUM_THREADS="1")
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
