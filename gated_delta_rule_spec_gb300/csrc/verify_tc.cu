@@ -322,6 +322,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         const size_t sh_hv = (size_t)slot * HV + hv, sh_h = (size_t)slot * H + h;
         const bool k_writer = (hv % P.G == 0) && vb == 0;
         bool waited = true;
+        // waits of this unit that ran out (bit per barrier: Gram, v history,
+        // checkpoint tile, output MMA)
+        uint32_t lost = 0;
         int f_slot = -1, f_wp = 0, f_base = 0;   // the next unit's fetch (thread 32)
         if (ok && tid == 32 && un < nunits) {     // fetch stage 1: the slot index
             int bbn, hvn, vbn;
@@ -454,6 +457,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             __syncthreads();
             waited = ptx::mbar_wait(bar_gram, ph_gram);
             ph_gram ^= 1u;
+            if (!waited) lost |= 1u;
             ptx::tc_fence_after_sync();
             if (tid == 32 && f_slot >= 0 && f_slot < C.num_slots) {  // fetch stage 2: cursors
                 f_wp = C.write_pos[f_slot];
@@ -662,6 +666,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             if (W > 0) {
                 vh_ok = ptx::mbar_wait(bar_vh, ph_vh);
                 ph_vh ^= 1u;
+                if (!vh_ok) lost |= 2u;
             }
             if (vrow < V) {
 #pragma unroll 4
@@ -718,6 +723,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         if (ok) {
             waited = ptx::mbar_wait(bar_s0, ph_s0);
             ph_s0 ^= 1u;
+            if (!waited) lost |= 4u;
             if (tid == 0) {
                 if (!waited) {
                     misc[5] = 1;
@@ -735,8 +741,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 }
                 ptx::mma_commit(bar_p);
             }
-            waited = ptx::mbar_wait(bar_p, ph_p) && waited;
+            const bool p_done = ptx::mbar_wait(bar_p, ph_p);
             ph_p ^= 1u;
+            if (!p_done) lost |= 8u;
+            waited = p_done && waited;
             ptx::tc_fence_after_sync();
             float pr[16];
             ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + kPCol, pr);
@@ -753,11 +761,23 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
         cur = nxt;
         // the tile and TMEM columns are reused by the next unit
         ptx::tc_fence_before_sync();
-        __syncthreads();
+        const int stop = __syncthreads_or(lost != 0);
         ptx::tc_fence_after_sync();
+        if (stop) {
+            // a wait ran out (the status bit is set below): give every copy or
+            // MMA this thread saw unfinished one more bounded wait, so that
+            // none still writes this CTA's shared memory or TMEM, and leave
+            if (tid == 0) misc[5] = 1;
+            if (lost & 1u) ptx::mbar_wait(bar_gram, ph_gram ^ 1u);
+            if (lost & 2u) ptx::mbar_wait(bar_vh, ph_vh ^ 1u);
+            if (lost & 4u) ptx::mbar_wait(bar_s0, ph_s0 ^ 1u);
+            if (lost & 8u) ptx::mbar_wait(bar_p, ph_p ^ 1u);
+            break;
+        }
     }
 
-    // ---- teardown: every TMEM read is complete; free the columns
+    // ---- teardown (also after a wait ran out): every TMEM read is
+    //      complete; free the columns
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (tid == 0 && misc[5]) atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
