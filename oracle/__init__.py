@@ -17,8 +17,12 @@ Every array here is fp64 in the same index order as the device layout:
 The method is the GDN recurrence ``S_t = exp(g_t) S_{t-1} (I - b_t k_t k_t^T) +
 b_t v_t k_t^T``, ``o_t = S_t q_t`` with L2-normalised q, k (sglang PR #28695
 "GDN ReplaySSM Ring Spec-Verify" and the blog post explaining it, §12.1), run
-token by token in fp64.  Parity of every function is pinned in
-``tests/test_oracle_pins.py``; none is marked "parity unpinned".
+token by token in fp64.  Parity of every function is pinned against something
+other than the oracle itself: verify, commit, fold and reset in
+``tests/test_oracle_pins.py`` and ``tests/test_cursor_protocol.py``, prefill in
+``tests/test_oracle_prefill_pins.py``, the snapshot comparison in
+``tests/test_oracle_snapshot_pins.py``; planted mistakes that the pins must catch
+are in ``tests/test_oracle_mutations.py``.  None is marked "parity unpinned".
 """
 from __future__ import annotations
 

@@ -12,6 +12,8 @@ import pytest
 import oracle
 from tests import test_cursor_protocol as cp
 from tests import test_oracle_pins as pins
+from tests import test_oracle_prefill_pins as pp
+from tests import test_oracle_snapshot_pins as sp
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_oracle.c")
 
@@ -34,6 +36,32 @@ MUTATIONS = {
     "history_off_by_one": ("for (int o = 0; o < W; ++o) {", "for (int o = 1; o < W; ++o) {"),
     "kda_gate_scalar": ("for (int j = 0; j < K; ++j) S[(size_t)i * K + j] *= exp(g[j]);",
                         "for (int j = 0; j < K; ++j) S[(size_t)i * K + j] *= exp(g[0]);"),
+    "prefill_keeps_base": (
+        "        if (!prefill_row_ok(d, cur, slot, from_zero, &st)) continue;\n"
+        "        cur->write_pos[slot] = 0;\n"
+        "        cur->cache_base[slot] = 0;\n",
+        "        if (!prefill_row_ok(d, cur, slot, from_zero, &st)) continue;\n"
+        "        cur->write_pos[slot] = 0;\n"),
+    "prefill_ignores_from_zero": ("if (J->from_zero) memset(S, 0, sizeof(double) * (size_t)V * K);",
+                                  "(void)0;"),
+    "prefill_reads_out_before_step": (
+        "        orc_step(V, K, d->per_key_gate, S, J->v + (tok * HV + hv) * V, J->k + (tok * H + h) * K, g,\n"
+        "                 beta, d->l2_eps);\n"
+        "        orc_readout(V, K, S, J->q + (tok * H + h) * K, d->l2_eps, d->scale, J->out + (tok * HV + hv) * V);\n",
+        "        orc_readout(V, K, S, J->q + (tok * H + h) * K, d->l2_eps, d->scale, J->out + (tok * HV + hv) * V);\n"
+        "        orc_step(V, K, d->per_key_gate, S, J->v + (tok * HV + hv) * V, J->k + (tok * H + h) * K, g,\n"
+        "                 beta, d->l2_eps);\n"),
+    "snapshot_commits_last_draft": ("snap + (((size_t)bb * T + acc - 1) * HV + hv) * VK",
+                                    "snap + (((size_t)bb * T + T - 1) * HV + hv) * VK"),
+    "snapshot_stores_state_before_step": (
+        "                orc_step(V, K, d->per_key_gate, S, v + (tok * HV + hv) * V, k + (tok * H + h) * K, g,\n"
+        "                         orc_gate_beta(b[tok * HV + hv]), d->l2_eps);\n"
+        "                orc_readout(V, K, S, q + (tok * H + h) * K, d->l2_eps, d->scale, out + (tok * HV + hv) * V);\n"
+        "                memcpy(snap + (tok * HV + hv) * VK, S, sizeof(double) * VK);\n",
+        "                memcpy(snap + (tok * HV + hv) * VK, S, sizeof(double) * VK);\n"
+        "                orc_step(V, K, d->per_key_gate, S, v + (tok * HV + hv) * V, k + (tok * H + h) * K, g,\n"
+        "                         orc_gate_beta(b[tok * HV + hv]), d->l2_eps);\n"
+        "                orc_readout(V, K, S, q + (tok * H + h) * K, d->l2_eps, d->scale, out + (tok * HV + hv) * V);\n"),
 }
 
 CHECKS = [
@@ -48,6 +76,13 @@ CHECKS = [
     lambda: cp.test_oracle_cursors_follow_protocol_b(16, 4),
     cp.test_golden_ring_walk_l8,
     cp.test_golden_margin_rule,
+    lambda: pp.test_prefill_equals_dense_recurrence(False, True),
+    lambda: pp.test_prefill_equals_dense_recurrence(True, False),
+    pp.test_prefill_in_two_calls_equals_one_call_bitwise,
+    pp.test_prefill_status_padding_and_unfolded_rows,
+    lambda: sp.test_snapshot_verify_equals_dense_recurrence(False),
+    sp.test_snapshot_commit_copies_the_accepted_state,
+    sp.test_snapshot_and_ring_agree_on_outputs_and_committed_state,
 ]
 
 
