@@ -82,6 +82,15 @@ def kernel_source_hash(path_name: str = "tc") -> str:
     return h.hexdigest()[:16]
 
 
+# Arithmetic of each path (the JSON line's "dtype" is the arithmetic type; bf16 is
+# only the type of the inputs and outputs).
+ARITH = {
+    "tc": "fp32; the Gram and the checkpoint product on tensor cores with tf32 operands "
+          "and fp32 accumulation",
+    "generic": "fp32 on CUDA cores",
+}
+
+
 def profiled_traffic(path_name: str, B: int, T: int):
     """DRAM bytes per verify launch from the committed ncu summary, if it was
     taken on the current verify source and the same window; else None."""
@@ -431,9 +440,10 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
-        "config": wl.config({"verify_kernel": path, "mean_ring_fill_W": round(mean_W, 2)}),
+        "config": wl.config({"verify_kernel": path, "arith": ARITH[path],
+                             "mean_ring_fill_W": round(mean_W, 2)}),
         "e2e": {"value": round(world * wl.B * wl.T * K_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": K_e2e,
@@ -612,9 +622,10 @@ def run_snapshot(args, rank: int, world: int) -> dict | None:
         "metric": METRIC, "variant": "snapshot (comparison: per-draft full states, no ring)",
         "value": round(world * wl.B * wl.T / t_step, 1), "unit": UNIT, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms / steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
         "config": wl.config({"workload": wl.name.replace("-verify-", "-snapshot-verify-"),
+                             "arith": ARITH["generic"],
                              "step": "snapshot verify + snapshot commit",
                              "snapshot_bytes": int(snap.numel() * 4)}),
         "gpu_launches": 2 * steps,
@@ -735,10 +746,11 @@ def run_prefill(args, rank: int, world: int) -> dict | None:
     return {
         "metric": PREFILL_METRIC, "value": round(world * B * N / t_call, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": calls, "warmup": args.warmup, "ms_per_step": round(ms / calls, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
         "config": {"workload": f"qwen3next-gdn-prefill-b{B}-n{N}", "B": B, "N": N, "H": wl.H,
                    "HV": wl.HV, "K": wl.K, "V": wl.V, "io_dtype": "bf16", "state_dtype": "fp32",
+                   "arith": ARITH["generic"],
                    "step": "prefill from a zero state (outputs, checkpoint, cursor reset)",
                    "parallelism": "replicas"},
         "e2e": {"value": round(world * B * N * K_e2e / (e2e_ms / 1e3), 1), "unit": "tokens/s",
