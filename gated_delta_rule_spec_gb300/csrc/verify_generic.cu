@@ -127,43 +127,75 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
     IO *rawk_w = reinterpret_cast<IO *>(P.rawk);
     IO *rawv_w = reinterpret_cast<IO *>(P.rawv);
     const bool k_writer = (hv % P.G == 0) && vb == 0;
-    if (tid == 0) {   // the checkpoint tile and the v history into L2 now; read at the end
+    if (tid == 0) {   // the history and the checkpoint tile into L2 now, ahead of their reads
+        // the ring history is one or two contiguous segments of each array
+        const int first = (L - base) < W ? (L - base) : W;
+        if (first > 0)
+            ptx::prefetch_l2(rawk + (sh_h * L + base) * K, (uint32_t)(first * K * sizeof(IO)));
+        if (W > first) ptx::prefetch_l2(rawk + sh_h * L * K, (uint32_t)((W - first) * K * sizeof(IO)));
+        if (KDA) {   // one gate per key channel: K floats per record
+            if (first > 0) ptx::prefetch_l2(P.ring_g + (sh_hv * L + base) * K, (uint32_t)first * K * 4);
+            if (W > first) ptx::prefetch_l2(P.ring_g + sh_hv * L * K, (uint32_t)(W - first) * K * 4);
+        }
         const int rows = V - v0 < kGenThreads ? V - v0 : kGenThreads;
         ptx::prefetch_l2(P.checkpoint + (sh_hv * V + v0) * K, (uint32_t)rows * K * 4);
-        if (V == kGenThreads) {   // whole records are contiguous: one or two segments
-            const int first = (L - base) < W ? (L - base) : W;
+        if (V == kGenThreads) {   // whole v records are contiguous
             if (first > 0)
                 ptx::prefetch_l2(rawv + (sh_hv * L + base) * V, (uint32_t)(first * V * sizeof(IO)));
             if (W > first) ptx::prefetch_l2(rawv + sh_hv * L * V, (uint32_t)((W - first) * V * sizeof(IO)));
         }
     }
 
-    // ---- 1. keys (history + window) and window queries, L2-normalised into X
-    for (int j = warp; j < n + T; j += kGenThreads / 32) {
-        const IO *src;
-        if (j < W)
-            src = rawk + (sh_h * L + ring_pos(base, j, L)) * K;
-        else if (j < n)
-            src = k + (((size_t)bb * T + (j - W)) * H + h) * K;
-        else
-            src = q + (((size_t)bb * T + (j - n)) * H + h) * K;
-        float ss = 0.0f;
-        for (int kk = lane; kk < K; kk += 32) {
-            float x = to_f32<IO>(src[kk]);
-            X[j * KP + kk] = x;
-            ss += x * x;
-        }
-        ss = warp_sum(ss);
-        const float r = 1.0f / sqrtf(ss + P.l2_eps);
-        for (int kk = lane; kk < K; kk += 32) X[j * KP + kk] *= r;
-        if (j >= W && j < n && k_writer) {  // side channel: raw key, bitwise
-            IO *dst = rawk_w + (sh_h * L + ring_pos(base, j, L)) * K;
-            for (int kk = lane; kk < K; kk += 32) dst[kk] = src[kk];
+    // ---- 1. keys (history + window) and window queries, L2-normalised into X.
+    //         A warp takes four rows at a time (rows jb .. jb + 3) and issues the
+    //         loads of all four before it uses any of them.
+    {
+        constexpr int kRows = 4, kPerLane = 4;   // K <= 128: four values per lane and row
+        for (int jb = warp * kRows; jb < n + T; jb += kRows * (kGenThreads / 32)) {
+            const IO *src[kRows];
+            float xv[kRows][kPerLane];
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) {
+                const int j = jb + rr;
+                src[rr] = nullptr;
+                if (j < W)
+                    src[rr] = rawk + (sh_h * L + ring_pos(base, j, L)) * K;
+                else if (j < n)
+                    src[rr] = k + (((size_t)bb * T + (j - W)) * H + h) * K;
+                else if (j < n + T)
+                    src[rr] = q + (((size_t)bb * T + (j - n)) * H + h) * K;
+            }
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr)
+#pragma unroll
+                for (int c = 0; c < kPerLane; ++c) {
+                    const int kk = lane + 32 * c;
+                    xv[rr][c] = (src[rr] != nullptr && kk < K) ? to_f32<IO>(src[rr][kk]) : 0.0f;
+                }
+#pragma unroll
+            for (int rr = 0; rr < kRows; ++rr) {
+                const int j = jb + rr;
+                if (j >= n + T) break;   // the same in every lane of the warp
+                float ss = 0.0f;
+#pragma unroll
+                for (int c = 0; c < kPerLane; ++c) ss = fmaf(xv[rr][c], xv[rr][c], ss);
+                ss = warp_sum(ss);
+                const float r = 1.0f / sqrtf(ss + P.l2_eps);
+#pragma unroll
+                for (int c = 0; c < kPerLane; ++c) {
+                    const int kk = lane + 32 * c;
+                    if (kk < K) X[j * KP + kk] = xv[rr][c] * r;
+                }
+                if (j >= W && j < n && k_writer) {  // side channel: raw key, bitwise
+                    IO *dst = rawk_w + (sh_h * L + ring_pos(base, j, L)) * K;
+                    for (int kk = lane; kk < K; kk += 32) dst[kk] = src[rr][kk];
+                }
+            }
         }
     }
     // ---- 2. gates: history from the ring, window computed (and written to the ring)
-    if (KDA) {   // n K gates: eight loads in flight per thread before any is used
-        constexpr int kB = 8;
+    if (KDA) {   // n K gates: sixteen loads in flight per thread before any is used
+        constexpr int kB = 16;
         for (int idx0 = tid; idx0 < n * K; idx0 += kB * kGenThreads) {
             float raw[kB];
 #pragma unroll
@@ -336,9 +368,10 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
     __syncthreads();
 
     // ---- 6. o_s = scale (S0 q_eff_s + sum_j c[s, j] v_j) for this thread's row;
-    //         global reads in batches of eight, so that a batch costs one round trip
+    //         global reads in batches (eight 16-byte checkpoint chunks, sixteen
+    //         values), so that a batch costs one round trip
     if (vrow < V) {
-        constexpr int kBatch = 8;
+        constexpr int kBatch = 8, kVBatch = 16;
         float acc[kGenMaxT];
 #pragma unroll
         for (int s = 0; s < kGenMaxT; ++s) acc[s] = 0.0f;
@@ -359,10 +392,10 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
                 }
             }
         }
-        for (int j0 = 0; j0 < n; j0 += kBatch) {
-            float vj[kBatch];
+        for (int j0 = 0; j0 < n; j0 += kVBatch) {
+            float vj[kVBatch];
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
+            for (int u = 0; u < kVBatch; ++u) {
                 const int j = j0 + u;
                 vj[u] = 0.0f;
                 if (j < W)
@@ -371,7 +404,7 @@ verify_generic_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slo
                     vj[u] = to_f32<IO>(v[(((size_t)bb * T + (j - W)) * HV + hv) * V + vrow]);
             }
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) {
+            for (int u = 0; u < kVBatch; ++u) {
                 if (j0 + u < n) {
 #pragma unroll
                     for (int s = 0; s < kGenMaxT; ++s)
