@@ -21,7 +21,8 @@ token by token in fp64.  Parity of every function is pinned against something
 other than the oracle itself: verify, commit, fold and reset in
 ``tests/test_oracle_pins.py`` and ``tests/test_cursor_protocol.py``, prefill in
 ``tests/test_oracle_prefill_pins.py``, the snapshot comparison in
-``tests/test_oracle_snapshot_pins.py``; planted mistakes that the pins must catch
+``tests/test_oracle_snapshot_pins.py``, the window's corrected deltas
+(``verify_d``) in ``tests/test_oracle_derived_d_pins.py``; planted mistakes that the pins must catch
 are in ``tests/test_oracle_mutations.py``.  None is marked "parity unpinned".
 """
 from __future__ import annotations
@@ -106,6 +107,8 @@ def _load(path: str | None = None):
                                      ctypes.c_double, P]
         _lib.orc_verify.restype = ctypes.c_uint32
         _lib.orc_verify.argtypes = [P, P, P, P, ctypes.c_int] + [P] * 8 + [P, ctypes.c_int]
+        _lib.orc_verify_d.restype = ctypes.c_uint32
+        _lib.orc_verify_d.argtypes = [P, P, P, P, ctypes.c_int] + [P] * 8 + [P, ctypes.c_int]
         _lib.orc_commit.restype = ctypes.c_uint32
         _lib.orc_commit.argtypes = [P, P, P, ctypes.c_int, P]
         _lib.orc_fold.restype = ctypes.c_uint32
@@ -312,6 +315,26 @@ def verify(dims: Dims, layer: Layer, cursors: Cursors, slot_idx, q, k, v, a, b, 
                             _ptr(slot_idx), B, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
                             _ptr(A_log), _ptr(dt_bias), _ptr(out), _ptr(mask), int(nthreads))
     return out, int(st)
+
+
+def verify_d(dims: Dims, layer: Layer, cursors: Cursors, slot_idx, q, k, v, a, b, A_log,
+             dt_bias, nthreads: int = 1):
+    """verify() that also returns the corrected delta of every window token:
+    (out [B,T,HV,V], d [B,T,HV,V], status bits), with d_t = beta_t (v_t - S k^_t)
+    taken against the decayed state before token t (blog post on sglang PR
+    #28695, §12.1).  These are what a ring caching d instead of raw v (the
+    derived-d design) would hold for the window's records."""
+    slot_idx = _i32(slot_idx)
+    B = slot_idx.shape[0]
+    q, k, v, a, b = _f64(q), _f64(k), _f64(v), _f64(a), _f64(b)
+    A_log, dt_bias = _f64(A_log), _f64(dt_bias)
+    out = np.zeros((B, dims.T, dims.HV, dims.V), np.float64)
+    dwin = np.zeros((B, dims.T, dims.HV, dims.V), np.float64)
+    cd, cl, cc = dims._c(), layer._c(), cursors._c()
+    st = _load().orc_verify_d(ctypes.byref(cd), ctypes.byref(cl), ctypes.byref(cc),
+                              _ptr(slot_idx), B, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                              _ptr(A_log), _ptr(dt_bias), _ptr(out), _ptr(dwin), int(nthreads))
+    return out, dwin, int(st)
 
 
 def commit(dims: Dims, cursors: Cursors, slot_idx, accept_len) -> int:

@@ -95,8 +95,11 @@ void orc_l2norm(int n, const double *x, double eps, double *out)
 
 /* g points to one value (GDN) or K values (KDA). k_raw is the raw key;
  * it is L2-normalised here, as the kernel does with the in-kernel norm. */
-void orc_step(int V, int K, int per_key_gate, double *S, const double *v,
-              const double *k_raw, const double *g, double beta, double eps)
+/* One step of the recurrence on S [V][K]; when d_out is not NULL it receives
+ * the corrected delta d [V] of the step ([blog] §12.1). */
+static void step_impl(int V, int K, int per_key_gate, double *S, const double *v,
+                      const double *k_raw, const double *g, double beta, double eps,
+                      double *d_out)
 {
     double *kh = (double *)malloc(sizeof(double) * (size_t)K);
     orc_l2norm(K, k_raw, eps, kh);
@@ -114,8 +117,15 @@ void orc_step(int V, int K, int per_key_gate, double *S, const double *v,
         for (int j = 0; j < K; ++j) u += row[j] * kh[j];
         double d = beta * (v[i] - u);
         for (int j = 0; j < K; ++j) row[j] += d * kh[j];
+        if (d_out) d_out[i] = d;
     }
     free(kh);
+}
+
+void orc_step(int V, int K, int per_key_gate, double *S, const double *v,
+              const double *k_raw, const double *g, double beta, double eps)
+{
+    step_impl(V, K, per_key_gate, S, v, k_raw, g, beta, eps, NULL);
 }
 
 /* o = scale * S q^ */
@@ -165,6 +175,7 @@ typedef struct {
     int B;
     const double *q, *k, *v, *a, *b, *A_log, *dt_bias;
     double *out;
+    double *dwin;              /* [B, T, HV, V] or NULL: the window's corrected deltas */
     const uint8_t *unit_mask;  /* [B*HV] or NULL: which (row, v-head) units to compute */
     uint32_t *row_status;      /* [B] */
     int next_unit;
@@ -207,8 +218,10 @@ static void verify_unit(verify_job *J, int bb, int hv)
     int slot = J->slot_idx[bb];
     uint32_t st = 0;
     if (!row_ok(d, J->cur, slot, &st)) {
-        for (int s = 0; s < T; ++s)
+        for (int s = 0; s < T; ++s) {
             memset(o_row0 + (((size_t)bb * T + s) * HV + hv) * V, 0, sizeof(double) * V);
+            if (J->dwin) memset(J->dwin + (((size_t)bb * T + s) * HV + hv) * V, 0, sizeof(double) * V);
+        }
         return;
     }
     const int base = J->cur->cache_base[slot];
@@ -231,8 +244,9 @@ static void verify_unit(verify_job *J, int bb, int hv)
         size_t tok = (size_t)bb * T + s;
         double beta;
         window_gate(J, bb, s, hv, g, &beta);
-        orc_step(V, K, d->per_key_gate, S, J->v + (tok * HV + hv) * V,
-                 J->k + (tok * H + h) * K, g, beta, d->l2_eps);
+        step_impl(V, K, d->per_key_gate, S, J->v + (tok * HV + hv) * V,
+                  J->k + (tok * H + h) * K, g, beta, d->l2_eps,
+                  J->dwin ? J->dwin + (tok * HV + hv) * V : NULL);
         orc_readout(V, K, S, J->q + (tok * H + h) * K, d->l2_eps, d->scale,
                     o_row0 + (tok * HV + hv) * V);
     }
@@ -299,19 +313,17 @@ static void verify_ring_write(verify_job *J)
     free(g);
 }
 
-/* Returns the OR of the status bits of all rows. */
-uint32_t orc_verify(const orc_dims *d, orc_layer *ly, const orc_cursors *cur,
-                    const int32_t *slot_idx, int B,
-                    const double *q, const double *k, const double *v,
-                    const double *a, const double *b,
-                    const double *A_log, const double *dt_bias,
-                    double *out, const uint8_t *unit_mask, int nthreads)
+static uint32_t verify_run(const orc_dims *d, orc_layer *ly, const orc_cursors *cur,
+                           const int32_t *slot_idx, int B, const double *q, const double *k,
+                           const double *v, const double *a, const double *b,
+                           const double *A_log, const double *dt_bias, double *out,
+                           double *dwin, const uint8_t *unit_mask, int nthreads)
 {
     verify_job J;
     memset(&J, 0, sizeof J);
     J.d = d; J.ly = ly; J.cur = cur; J.slot_idx = slot_idx; J.B = B;
     J.q = q; J.k = k; J.v = v; J.a = a; J.b = b; J.A_log = A_log; J.dt_bias = dt_bias;
-    J.out = out; J.unit_mask = unit_mask;
+    J.out = out; J.dwin = dwin; J.unit_mask = unit_mask;
     pthread_mutex_init(&J.lock, NULL);
     if (nthreads < 1) nthreads = 1;
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
@@ -324,6 +336,34 @@ uint32_t orc_verify(const orc_dims *d, orc_layer *ly, const orc_cursors *cur,
     uint32_t st = 0;
     for (int bb = 0; bb < B; ++bb) row_ok(d, cur, slot_idx[bb], &st);
     return st;
+}
+
+/* Returns the OR of the status bits of all rows. */
+uint32_t orc_verify(const orc_dims *d, orc_layer *ly, const orc_cursors *cur,
+                    const int32_t *slot_idx, int B,
+                    const double *q, const double *k, const double *v,
+                    const double *a, const double *b,
+                    const double *A_log, const double *dt_bias,
+                    double *out, const uint8_t *unit_mask, int nthreads)
+{
+    return verify_run(d, ly, cur, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, NULL,
+                      unit_mask, nthreads);
+}
+
+/* Verify that also returns the corrected delta d [B, T, HV, V] of every window
+ * token: d = beta (v - S k^) against the decayed state before the token
+ * ([blog] §12.1).  These are the values a ring that caches d (the derived-d
+ * design of [blog] appendix A.1) would hold for the window's records; rows
+ * that are not computed read zeros. */
+uint32_t orc_verify_d(const orc_dims *d, orc_layer *ly, const orc_cursors *cur,
+                      const int32_t *slot_idx, int B,
+                      const double *q, const double *k, const double *v,
+                      const double *a, const double *b,
+                      const double *A_log, const double *dt_bias,
+                      double *out, double *dwin, int nthreads)
+{
+    return verify_run(d, ly, cur, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, dwin, NULL,
+                      nthreads);
 }
 
 /* ------------------------------------------------------------------ */

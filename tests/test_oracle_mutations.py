@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from tests import test_cursor_protocol as cp
+from tests import test_oracle_derived_d_pins as dd
 from tests import test_oracle_pins as pins
 from tests import test_oracle_prefill_pins as pp
 from tests import test_oracle_snapshot_pins as sp
@@ -51,6 +52,7 @@ MUTATIONS = {
         "        orc_readout(V, K, S, J->q + (tok * H + h) * K, d->l2_eps, d->scale, J->out + (tok * HV + hv) * V);\n"
         "        orc_step(V, K, d->per_key_gate, S, J->v + (tok * HV + hv) * V, J->k + (tok * H + h) * K, g,\n"
         "                 beta, d->l2_eps);\n"),
+    "window_d_without_state": ("if (d_out) d_out[i] = d;", "if (d_out) d_out[i] = beta * v[i];"),
     "snapshot_commits_last_draft": ("snap + (((size_t)bb * T + acc - 1) * HV + hv) * VK",
                                     "snap + (((size_t)bb * T + T - 1) * HV + hv) * VK"),
     "snapshot_stores_state_before_step": (
@@ -83,6 +85,8 @@ CHECKS = [
     lambda: sp.test_snapshot_verify_equals_dense_recurrence(False),
     sp.test_snapshot_commit_copies_the_accepted_state,
     sp.test_snapshot_and_ring_agree_on_outputs_and_committed_state,
+    lambda: dd.test_window_d_equals_closed_form_and_rank_one_identity(True, 3),
+    lambda: dd.test_state_reconstructed_from_checkpoint_and_deltas(False),
 ]
 
 

@@ -152,7 +152,7 @@ def _window(rng, d: oracle.Dims, B, io=gen.FP32):
         dt_bias.astype(np.float64)
 
 
-def _ut_closed_form(d, S0, hist, win_k, win_v, win_q, win_g, win_beta):
+def _ut_closed_form(d, S0, hist, win_k, win_v, win_q, win_g, win_beta, with_d=False):
     """Closed-form chunked UT transform of one (row, v-head) unit.
 
     Tokens 0..n-1 = W history records then T window tokens.  With per-token
@@ -163,7 +163,7 @@ def _ut_closed_form(d, S0, hist, win_k, win_v, win_q, win_g, win_beta):
         o_s     = Gamma[s, -1] S0 q^_s + sum_{r <= s} Gamma[s, r] <k^_r, q^_s> d_r
     For KDA the decays are per key channel and sit inside the inner products.
     Returns outputs [T, V] computed with an explicit inverse (numpy) and with
-    the exact finite Neumann sum of the nilpotent A.
+    the exact finite Neumann sum of the nilpotent A; with_d: also D by both.
     """
     ks = [*hist["k"], *win_k]
     vs = [*hist["v"], *win_v]
@@ -200,6 +200,8 @@ def _ut_closed_form(d, S0, hist, win_k, win_v, win_q, win_g, win_beta):
                 o = o + np.sum(kh[r] * qh[s] * decay(i, r)) * D[r]
             O[s] = d.scale * o
         outs.append(O)
+    if with_d:
+        return outs, (D_inv, D_neu)
     return outs
 
 
