@@ -114,6 +114,17 @@ def test_tc_fold_deferred_until_the_ring_is_full():
     assert binding.read_status(sc.cur) == 0
 
 
+def test_generic_two_v_blocks_fp32():
+    """The CUDA-core kernel over V = 160: a full and a partial block of 128 state
+    rows (and fold items of 64, 64 and 32 rows)."""
+    wl = gen.Workload("generic-v160", B=2, H=1, HV=2, K=64, V=160, T=3, L=16, io_dtype=gen.FP32,
+                      prefix=8)
+    sc = Scenario(wl, B=2, seed=41, num_slots=3)
+    assert binding.verify_path(sc.layer) == "generic"
+    worst = _rounds(sc, 12, full_frac=0.3)
+    assert worst["out"] <= 1e-4
+
+
 def test_c1_weak_decay_heads():
     """Weak decays (a shifted down by 4) make the checkpoint and the whole ring
     history matter for every output."""
