@@ -81,7 +81,9 @@ extern "C" {
 #define GDN_SPEC_ST_SLOT_OOR       2u  /* slot_idx[b] >= num_slots                        */
 #define GDN_SPEC_ST_RING_OVERFLOW  4u  /* verify: write_pos + T > L (a fold was skipped)  */
 #define GDN_SPEC_ST_CURSOR_CORRUPT 8u  /* write_pos < 0, write_pos > L or cache_base outside [0, L) */
-#define GDN_SPEC_ST_TIMEOUT       16u  /* a bounded device wait ran out (that call's outputs are invalid) */
+#define GDN_SPEC_ST_TIMEOUT       16u  /* a bounded device wait ran out: that call's outputs are invalid
+                                              (the CTA that saw it drains its copies and stops, so rows it
+                                              had not reached keep whatever `out` held) */
 #define GDN_SPEC_ST_UNFOLDED      32u  /* prefill: continuing from a checkpoint whose ring is not folded */
 
 #define GDN_SPEC_GATE_SCALAR  0    /* GDN: one gate per (token, v-head)            */
