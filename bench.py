@@ -800,8 +800,9 @@ def prefill_cpu(B: int, N: int, seconds: float = 10.0) -> dict:
 # ----------------------------------------------------------------- reference arm
 
 def run_reference(args, rank: int, world: int) -> dict | None:
-    """fp64 oracle steps (verify -> commit -> fold) on a bounded sample of the
-    workload's rows, timed on the host cores."""
+    """fp64 oracle steps (verify -> commit -> fold; with --variant snapshot,
+    snapshot verify -> snapshot commit) on a bounded sample of the workload's
+    rows, timed on the host cores."""
     if rank != 0:
         return None
     import oracle
@@ -827,8 +828,15 @@ def run_reference(args, rank: int, world: int) -> dict | None:
             for _ in range(4)]
     accs = [gen.accept_lens(rng, rows, c.T) for _ in range(4)]
 
+    snapshot = args.variant == "snapshot"
+
     def step(i):
         w = wins[i % 4]
+        if snapshot:
+            _, snap, _ = oracle.snapshot_verify(d, ly, slot_idx, w["q"], w["k"], w["v"], w["a"],
+                                                w["b"], A_log, dt)
+            oracle.snapshot_commit(d, ly, slot_idx, accs[i % 4], snap)
+            return
         oracle.verify(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
                       nthreads=cores)
         oracle.commit(d, cur, slot_idx, accs[i % 4])
@@ -841,13 +849,17 @@ def run_reference(args, rank: int, world: int) -> dict | None:
         step(i)
     el = time.perf_counter() - t0
     value = rows * c.T * args.steps / el
+    what = "snapshot verify + snapshot commit" if snapshot else "verify + commit + fold"
     sample = (f"{rows} rows x {c.HV} v-heads of the B={args.batch} workload per step "
-              f"(verify + commit + fold, fp64), {args.steps} steps")
+              f"({what}, fp64), {args.steps} steps")
+    extra = {"sample_rows_per_step": rows}
+    if snapshot:
+        extra.update(workload=wl.name.replace("-verify-", "-snapshot-verify-"), step=what)
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": wl.config({"sample_rows_per_step": rows}),
+            "config": wl.config(extra),
             "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
