@@ -119,3 +119,72 @@ def test_state_reconstructed_from_checkpoint_and_deltas(per_key):
                 gam = np.exp(logal[j + 1:].sum(axis=0))        # decay from token j to the end
                 rec = rec + np.outer(ds[j], _khat(np.asarray(ks[j])) * gam)
             np.testing.assert_allclose(rec, S[n], rtol=1e-10, atol=1e-12)
+
+
+def _verify_from_d_ring(d, ly, dring, cur, slot, hv, w, bb, A_log, dtb):
+    """One (row, v-head) unit of a verify that takes the history through the
+    cached deltas (the derived-d design): only the T x T window system is
+    solved.  Written here with dense numpy, independently of the oracle."""
+    T, L, V = d.T, d.L, d.V
+    h = hv // (d.HV // d.H)
+    base, W = cur.cache_base[slot], cur.write_pos[slot]
+    pos = [(base + o) % L for o in range(W)]
+    kh = [_khat(ly.rawk[slot, h, p]) for p in pos]
+    dh = [dring[slot, hv, p] for p in pos]
+    kw = [_khat(w["k"][bb, s, h]) for s in range(T)]
+    qw = [_khat(w["q"][bb, s, h]) for s in range(T)]
+    gw, bw = oracle.gate(A_log[hv:hv + 1], w["a"][bb, :, hv:hv + 1], dtb[hv:hv + 1],
+                         w["b"][bb, :, hv:hv + 1])
+    gw, bw = gw.reshape(-1), bw.reshape(-1)
+    cum = np.concatenate([[0.0], np.cumsum([ly.ring_g[slot, hv, p] for p in pos] + list(gw))])
+
+    def gam(i, r):   # decay over tokens r+1..i (r = -1: from the checkpoint)
+        return np.exp(cum[i + 1] - cum[r + 1])
+
+    S0 = ly.checkpoint[slot, hv]
+    Hk = [sum((gam(W + s, r) * (kh[r] @ kw[s]) * dh[r] for r in range(W)), np.zeros(V)) for s in range(T)]
+    Hq = [sum((gam(W + s, r) * (kh[r] @ qw[s]) * dh[r] for r in range(W)), np.zeros(V)) for s in range(T)]
+    R = np.array([bw[s] * (w["v"][bb, s, hv] - gam(W + s, -1) * (S0 @ kw[s]) - Hk[s]) for s in range(T)])
+    A = np.array([[bw[s] * gam(W + s, W + s2) * (kw[s2] @ kw[s]) if s2 < s else 0.0
+                   for s2 in range(T)] for s in range(T)])
+    Dw = np.linalg.solve(np.eye(T) + A, R)
+    out = np.array([d.scale * (gam(W + s, -1) * (S0 @ qw[s]) + Hq[s] +
+                               sum(gam(W + s, W + s2) * (kw[s2] @ qw[s]) * Dw[s2] for s2 in range(s + 1)))
+                    for s in range(T)])
+    return out, Dw
+
+
+def test_cached_deltas_reproduce_verify_over_rounds_with_folds():
+    """Keep the window d's that verify_d returns in a ring (at the window's ring
+    positions, as the raw records are kept), then verify -> commit -> fold for
+    many rounds: a verify that takes its history through those d's alone gives
+    the oracle's outputs and window d's.  Pins verify_d's deltas as the ones a
+    derived-d ring holds, across rejected drafts and folds."""
+    from gated_delta_rule_spec_gb300 import inputs as gen
+    rng = np.random.default_rng(3)
+    d = oracle.Dims(H=2, HV=4, K=16, V=8, T=4, L=16, num_slots=3, scale=0.9)
+    ly = oracle.Layer(d, checkpoint=rng.standard_normal((3, d.HV, d.V, d.K)) * 0.3)
+    dring = np.zeros((3, d.HV, d.L, d.V))
+    cur = oracle.Cursors(3)
+    slots = np.array([2, 0], np.int32)
+    A_log, dtb = (x.astype(np.float64) for x in gen.layer_params(rng, d.HV, d.K, False))
+    folds = 0
+    for _ in range(30):
+        w = {n: gen.to_f64(x) for n, x in
+             gen.window_inputs(rng, 2, d.T, d.H, d.HV, d.K, d.V, gen.BF16).items()}
+        w["a"] = w["a"] - 2.0
+        before, cur0 = ly.copy(), cur.copy()
+        o_orc, d_orc, st = oracle.verify_d(d, ly, cur, slots, w["q"], w["k"], w["v"], w["a"],
+                                           w["b"], A_log, dtb)
+        assert st == 0
+        for bb, slot in enumerate(slots):
+            for hv in range(d.HV):
+                o, dw = _verify_from_d_ring(d, before, dring, cur0, slot, hv, w, bb, A_log, dtb)
+                np.testing.assert_allclose(o, o_orc[bb, :, hv], rtol=1e-9, atol=1e-11)
+                np.testing.assert_allclose(dw, d_orc[bb, :, hv], rtol=1e-9, atol=1e-11)
+                for s in range(d.T):
+                    dring[slot, hv, (cur0.cache_base[slot] + cur0.write_pos[slot] + s) % d.L] = dw[s]
+        assert oracle.commit(d, cur, slots, gen.accept_lens(rng, 2, d.T)) == 0
+        folds += int(cur.is_flush[slots].sum())
+        assert oracle.fold(d, ly, cur, slots) == 0
+    assert folds > 0
