@@ -47,11 +47,3 @@ def test_kda_small_weak_decay_fp32():
     worst = _kda_rounds(sc, 25, ring_every=1)
     assert worst <= 1e-4
 
-
-def test_kda_window_of_eight_tokens():
-    """KDA with a draft window of eight tokens and K = V = 64, bf16."""
-    wl = gen.Workload("kda-t8", B=2, H=2, HV=4, K=64, V=64, T=8, L=32, per_key_gate=True,
-                      prefix=16)
-    sc = Scenario(wl, B=2, seed=13, num_slots=3, decay_shift=2.0)
-    assert binding.verify_path(sc.layer) == "generic"
-    _kda_rounds(sc, 15, ring_every=3)
