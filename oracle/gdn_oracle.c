@@ -381,7 +381,10 @@ uint32_t orc_commit(const orc_dims *d, orc_cursors *cur, const int32_t *slot_idx
         if (slot >= d->num_slots) { st |= ORC_ST_SLOT_OOR; continue; }
         int acc = accept_len[bb];
         if (acc < 0 || acc > d->T) { st |= ORC_ST_ACCEPT_RANGE; continue; }
-        int wp = cur->write_pos[slot] + acc;
+        /* cursors out of range (the same rule verify applies): skip the row */
+        int wp0 = cur->write_pos[slot], base = cur->cache_base[slot];
+        if (wp0 < 0 || wp0 > d->L || base < 0 || base >= d->L) { st |= ORC_ST_CURSOR_CORRUPT; continue; }
+        int wp = wp0 + acc;
         cur->write_pos[slot] = wp;
         cur->is_flush[slot] = (wp + 2 * d->T > d->L) ? 1 : 0;
     }

@@ -429,3 +429,20 @@ def test_commit_status_bits():
     assert list(cur.write_pos) == [0, 2]
     st = oracle.commit(d, cur, [0], [-1])
     assert st == oracle.ST_ACCEPT_RANGE
+
+
+def test_commit_skips_rows_with_corrupt_cursors():
+    """A row whose cursors are outside the ring (write_pos outside [0, L] or
+    cache_base outside [0, L), the rule verify applies) is left exactly as it is
+    and reported; the other rows commit normally."""
+    d = oracle.Dims(H=1, HV=1, K=2, V=2, T=4, L=16, num_slots=5)
+    cur = oracle.Cursors(5, write_pos=[-1, 17, 3, 16, 2], cache_base=[0, 0, 16, 15, -2],
+                         is_flush=[0, 0, 0, 1, 0])
+    before = cur.copy()
+    st = oracle.commit(d, cur, [0, 1, 2, 3, 4], [1, 1, 1, 0, 1])
+    assert st == oracle.ST_CURSOR_CORRUPT
+    for name in ("write_pos", "cache_base", "is_flush"):
+        got, want = getattr(cur, name), getattr(before, name)
+        assert list(got[[0, 1, 2, 4]]) == list(want[[0, 1, 2, 4]]), name
+    # the edge write_pos == L is in range: it commits (accept 0) and stays flagged
+    assert cur.write_pos[3] == 16 and cur.is_flush[3] == 1
