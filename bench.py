@@ -91,9 +91,12 @@ ARITH = {
 }
 
 
-def profiled_traffic(path_name: str, B: int, T: int):
-    """DRAM bytes per verify launch from the committed ncu summary, if it was
-    taken on the current verify source and the same window; else None."""
+def profiled_traffic(path_name: str, B: int, T: int, algorithmic_bytes: float):
+    """DRAM bytes per verify launch from the committed ncu record, if it was
+    taken on the current verify source and the same window; else None.  The
+    record holds DRAM bytes over algorithmic bytes of the profiled launches;
+    that ratio times this run's algorithmic bytes is the per-launch figure
+    (traffic grows with the units and the ring fill as the bytes do)."""
     f = os.path.join(ROOT, "profiles", f"verify_{path_name}_traffic.json")
     if not os.path.exists(f):
         return None
@@ -103,8 +106,10 @@ def profiled_traffic(path_name: str, B: int, T: int):
         return None
     if rec.get("kernel_source_hash") != kernel_source_hash(path_name) or rec.get("T") != T:
         return None
-    per_row = rec.get("dram_bytes_per_launch_per_row")
-    return None if per_row is None else float(per_row) * B
+    ratio = rec.get("dram_over_algorithmic")
+    if ratio is None:
+        return None
+    return round(float(ratio) * algorithmic_bytes)
 
 
 def measured_peaks():
@@ -317,19 +322,27 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     if world > 1:
         dist.barrier()
     ms = t_start.elapsed_time(t_end)
-    # per-verify durations of the last chunk replay inside the timed region
-    verify_ms = []
+    # per-verify durations sampled inside the timed region (every EV_EVERY-th step
+    # of the last chunk replay): a cross-check of the verify-only graph below
+    verify_ms_in_step = []
     if args.steps // R > 0 and ev is not None:
         try:
-            verify_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in ev_steps]
+            verify_ms_in_step = [ev[i][0].elapsed_time(ev[i][1]) for i in ev_steps]
         except RuntimeError:
-            verify_ms = []
-    if not verify_ms:
-        verify_ms = verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias)
+            verify_ms_in_step = []
     clocks = sampler.summary(wall0, wall1) if sampler else None
     if sampler:
         sampler.stop()
     status = binding.read_status(cur)
+    # the verify kernel on its own: median over 10 replays of a graph of 20
+    # back-to-back verify calls on the state the timed steps left (inputs rotate
+    # over 16 windows; the 256 MiB checkpoint working set is larger than L2)
+    W_now = cur.write_pos[slots.long()].cpu().numpy().astype(np.int64)
+    verify_graph_ms, verify_graph_all = verify_only_times(binding, layer, cur, slots, inputs, outs,
+                                                          A_log, dt_bias, n=20, reps=10)
+    graph_bytes = float(verify_bytes_per_unit(W_now, wl.K, wl.V, wl.T, wl.G, wl.e, wl.kda).sum()
+                        * wl.HV)
+    status |= binding.read_status(cur)
 
     # byte accounting for the verifies of the last chunk replay
     acc_seq = np.array([acc_np[i % R] for i in range(args.warmup)]
@@ -341,10 +354,12 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     W_last = W_all[last] if args.steps // R > 0 else W_all
     if args.steps // R > 0 and ev is not None:   # the verifies the events bracketed
         W_last = W_last[ev_steps]
-    bytes_per_launch = float(np.mean([
+    bytes_in_step = float(np.mean([
         verify_bytes_per_unit(Wr, wl.K, wl.V, wl.T, wl.G, wl.e, wl.kda).sum() * wl.HV
         for Wr in W_last]))
-    mean_W = float(W_last.mean())
+    mean_W = float(W_now.mean())
+    # committed tokens of the timed steps (sum of accept_len over rows)
+    committed = float(acc_seq[args.warmup:].sum()) * world
 
     # e2e through the binding with host buffers: every step copies its inputs
     # (q, k, v, a, b and accept_len, packed in one pinned buffer) to the device
@@ -434,9 +449,10 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     tokens = world * wl.B * wl.T * args.steps
     value = tokens / (ms / 1e3)
     peaks, peak_kind = measured_peaks()
-    v_ms = float(np.mean(verify_ms)) if verify_ms else float("nan")
-    achieved = bytes_per_launch / (v_ms / 1e3) / 1e9 if verify_ms else float("nan")
-    traffic = profiled_traffic(path, wl.B, wl.T)
+    v_ms = verify_graph_ms
+    achieved = graph_bytes / (v_ms / 1e3) / 1e9
+    v_step_ms = float(np.mean(verify_ms_in_step)) if verify_ms_in_step else None
+    traffic = profiled_traffic(path, wl.B, wl.T, graph_bytes)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
@@ -444,6 +460,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
         "config": wl.config({"verify_kernel": path, "arith": ARITH[path],
                              "mean_ring_fill_W": round(mean_W, 2)}),
+        "us_per_round": round(ms / args.steps * 1e3, 2),
+        "committed_tokens_per_s": round(committed / (ms / 1e3), 1),
         "e2e": {"value": round(world * wl.B * wl.T * K_e2e / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": K_e2e,
@@ -453,14 +471,48 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": round(bytes_per_launch),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": round(graph_bytes),
                      "kernel": f"verify ({path})", "peak_kind": peak_kind,
-                     "verify_us": round(v_ms * 1e3, 2)},
-        "verify_tokens_per_s": round(wl.B * wl.T / (v_ms / 1e3), 1) if verify_ms else None,
+                     "verify_us": round(v_ms * 1e3, 2),
+                     "verify_timing": "median of 10 replays of a CUDA graph of 20 back-to-back "
+                                      "verify calls, after the timed steps",
+                     "verify_us_replays": [round(x * 1e3, 2) for x in verify_graph_all],
+                     "verify_us_in_step": (round(v_step_ms * 1e3, 2) if v_step_ms else None),
+                     "algorithmic_bytes_per_launch_in_step": round(bytes_in_step)},
+        "verify_tokens_per_s": round(wl.B * wl.T / (v_ms / 1e3), 1),
         "device_status": status,
         "clocks": clocks,
     }
     return line
+
+
+def run_verify_only(args) -> dict:
+    """Profiling aid: the bench's state, then --steps plain verify calls (no
+    commit, so every call sees the same ring fill) and nothing else; prints the
+    algorithmic bytes of one call, so that DRAM counters taken on these launches
+    can be set against them."""
+    import torch
+    from gated_delta_rule_spec_gb300 import binding
+
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    binding.load()
+    wl = Workload(args.batch, args.window, args.kda)
+    rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 1000, device,
+                                                                     args.setup_rounds)
+    inputs = [dev_window() for _ in range(4)]
+    out = torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device)
+    W = cur.write_pos[slots.long()].cpu().numpy().astype(np.int64)
+    for i in range(args.steps):
+        w = inputs[i % 4]
+        binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias,
+                       out=out)
+    torch.cuda.synchronize()
+    byts = float(verify_bytes_per_unit(W, wl.K, wl.V, wl.T, wl.G, wl.e, wl.kda).sum() * wl.HV)
+    return {"mode": "verify-only", "workload": wl.name, "verify_kernel": binding.verify_path(layer),
+            "calls": args.steps, "setup_verify_calls": 16 + args.setup_rounds,
+            "algorithmic_bytes_per_launch": round(byts), "mean_ring_fill_W": round(float(W.mean()), 2),
+            "device_status": binding.read_status(cur)}
 
 
 def reduce_max(values, device="cpu"):
@@ -473,7 +525,8 @@ def reduce_max(values, device="cpu"):
 
 
 def verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias, n=20, reps=10):
-    """Median over replays of a graph of n back-to-back verify calls, per call (ms)."""
+    """Per-call time (ms) of a graph of n back-to-back verify calls: (median over
+    reps replays, every replay's value)."""
     import torch
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
@@ -494,12 +547,14 @@ def verify_only_times(binding, layer, cur, slots, inputs, outs, A_log, dt_bias, 
         b.record()
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b) / n)
-    return [statistics.median(times)]
+    return statistics.median(times), times
 
 
-def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None, kda: bool = False) -> dict:
+def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None, kda: bool = False,
+                 single_thread_seconds: float = 4.0) -> dict:
     """The fp64 oracle, as it stands, on the host cores: verify of a sample of
-    the workload's rows (all heads), ring fill W ~ U[0, L-2T] as in the sweep."""
+    the workload's rows (all heads), ring fill W ~ U[0, L-2T] as in the sweep;
+    then the same on one thread."""
     import oracle
     from gated_delta_rule_spec_gb300 import inputs as gen
 
@@ -521,18 +576,27 @@ def cpu_baseline(B: int, seconds: float = 10.0, T: int | None = None, kda: bool 
          gen.window_inputs(rng, rows, c.T, c.H, c.HV, c.K, c.V, gen.BF16, kda).items()}
     cores = os.cpu_count() or 1
     slot_idx = np.arange(rows, dtype=np.int32)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.verify(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
-                      nthreads=cores)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or reps >= 10000:
-            break
+
+    def timed(nthreads, secs, rows_used):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.verify(d, ly, cur, slot_idx[:rows_used], w["q"][:rows_used], w["k"][:rows_used],
+                          w["v"][:rows_used], w["a"][:rows_used], w["b"][:rows_used], A_log, dt,
+                          nthreads=nthreads)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= secs or reps >= 10000:
+                return reps, el
+
+    reps, el = timed(cores, seconds, rows)
+    reps1, el1 = timed(1, single_thread_seconds, 1)
     return {"value": round(rows * c.T * reps / el, 2), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{rows} rows x {c.HV} v-heads of the B={B} workload, fp64 verify, "
-                      f"{reps} repetitions in {el:.1f} s, W ~ U[0, {c.L - 2 * c.T}]"}
+                      f"{reps} repetitions in {el:.1f} s, W ~ U[0, {c.L - 2 * c.T}]",
+            "single_thread": {"value": round(c.T * reps1 / el1, 2), "unit": UNIT, "cores": 1,
+                              "sample": f"1 row x {c.HV} v-heads, {reps1} repetitions in "
+                                        f"{el1:.1f} s"}}
 
 
 # ----------------------------------------------------------------- snapshot comparison
@@ -884,6 +948,9 @@ def main():
                     help="snapshot: the per-draft state design the ring replaces (comparison)")
     ap.add_argument("--prefill", type=int, default=0, metavar="N",
                     help="measure gdn_spec_prefill of --batch prompts of N tokens instead")
+    ap.add_argument("--verify-only", action="store_true",
+                    help="profiling aid: build the state, run --steps plain verify calls, print "
+                         "their algorithmic bytes")
     ap.add_argument("--setup-rounds", type=int, default=48,
                     help="random rounds of the state build (fewer: a short run to profile)")
     args = ap.parse_args()
@@ -898,6 +965,9 @@ def main():
         if args.impl == "reference":
             backend = "gloo"
         dist.init_process_group(backend)
+    if args.verify_only:
+        print(json.dumps(run_verify_only(args)), flush=True)
+        return
     if args.prefill and args.impl == "reference":
         line = None
         if rank == 0:   # the oracle's prefill on the host cores, a bounded sample

@@ -52,7 +52,7 @@ _lib = None
 EXPORTS = ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset", "gdn_spec_prefill",
            "gdn_spec_snapshot_verify", "gdn_spec_snapshot_commit",
            "gdn_spec_read_status", "gdn_spec_strerror", "gdn_spec_abi_version",
-           "gdn_spec_verify_path")
+           "gdn_spec_verify_path", "gdn_spec_set_wait_limit")
 
 
 def library_path() -> str:
@@ -90,6 +90,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_spec_abi_version.restype = ctypes.c_int
     lib.gdn_spec_verify_path.argtypes = [LP]
     lib.gdn_spec_verify_path.restype = ctypes.c_char_p
+    lib.gdn_spec_set_wait_limit.argtypes = [ctypes.c_uint32]
+    lib.gdn_spec_set_wait_limit.restype = ctypes.c_uint32
     _lib = lib
     return lib
 
@@ -295,3 +297,13 @@ def read_status(cursors: SpecCursors, clear: bool = True, stream=None) -> int:
                                      _stream(stream))
     _check(rc, "gdn_spec_read_status")
     return int(v.value)
+
+
+WAIT_LIMIT_DEFAULT = 0xFFFFFFFF
+
+
+def set_wait_limit(polls: int) -> int:
+    """gdn_spec_set_wait_limit (diagnostic): polls after which the first wait on
+    each data copy gives up; WAIT_LIMIT_DEFAULT restores the default.  Returns
+    the previous limit."""
+    return int(load().gdn_spec_set_wait_limit(ctypes.c_uint32(polls & 0xFFFFFFFF)))

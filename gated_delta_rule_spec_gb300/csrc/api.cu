@@ -2,12 +2,20 @@
 // in include/gdn_spec.h): host-side validation, kernel selection and
 // stream-ordered launches.  Nothing here allocates, frees or synchronises,
 // except gdn_spec_read_status.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
 #include "common.cuh"
 
 namespace gdnspec {
+
+namespace {
+std::atomic<uint32_t> g_data_wait_limit{kWaitLimitDefault};
+}  // namespace
+
+uint32_t data_wait_limit() { return g_data_wait_limit.load(std::memory_order_relaxed); }
+
 cudaError_t launch_verify_generic(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
                                   const int32_t *slot_idx, int B, const void *q, const void *k,
                                   const void *v, const void *a, const void *b,
@@ -275,6 +283,10 @@ int gdn_spec_reset(const gdn_spec_cursors *cursors, const int32_t *slot_idx, int
     if (B == 0) return GDN_SPEC_OK;
     if (!slot_idx) return GDN_SPEC_EINVAL;
     return cuda_rc(launch_reset(cursor_args(cursors), slot_idx, B, static_cast<cudaStream_t>(stream)));
+}
+
+uint32_t gdn_spec_set_wait_limit(uint32_t polls) {
+    return g_data_wait_limit.exchange(polls == 0xFFFFFFFFu ? kWaitLimitDefault : polls);
 }
 
 int gdn_spec_read_status(const gdn_spec_cursors *cursors, uint32_t *host_out, int32_t clear,

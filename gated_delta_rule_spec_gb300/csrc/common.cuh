@@ -28,6 +28,19 @@ struct CursorArgs {
     uint32_t *status;
 };
 
+// is_flush value with which the fold marks a row it could not finish (a bounded
+// wait ran out); its cursor move then poisons the row (write_pos = -1).
+constexpr int kFoldFailed = 2;
+
+// Default iteration limit of a bounded mbarrier wait (about 0.3 s).
+constexpr uint32_t kWaitLimitDefault = 1u << 20;
+
+// Iteration limit of the first wait on each data copy (verify's checkpoint
+// tile, the fold's ring records, prefill's prompt chunks), set by
+// gdn_spec_set_wait_limit; the waits that drain copies after a failure always
+// use kWaitLimitDefault.
+uint32_t data_wait_limit();
+
 // Layers folded by one launch (the grid's z axis is layer * HV + v-head).
 constexpr int kFoldMaxLayers = 48;
 struct FoldLayers {

@@ -38,6 +38,11 @@
 // layers are independent here and one launch folds all of them (the blog's
 // §2.1 observation about replay outside the forward).  The cursors move in
 // a separate launch after every layer.
+//
+// When a bounded wait runs out, the item's row is marked (is_flush =
+// kFoldFailed) and the CTA goes on; the cursor move then poisons that row
+// instead of moving it, since some of its layers and v-heads may be folded
+// and others not.
 #include "common.cuh"
 #include "ptx_sm100.cuh"
 #include "replay.cuh"
@@ -78,7 +83,7 @@ size_t fold_smem_bytes(int K, int L, bool kda, bool bf16) {
 template <typename IO, bool KDA, int K>
 __global__ void __launch_bounds__(kFoldThreads, 4)
 fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
-            const int32_t *__restrict__ slot_idx, int B) {
+            const int32_t *__restrict__ slot_idx, int B, uint32_t wait_limit) {
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
     constexpr int kPer = KC::kVals;                 // key values per 16-byte chunk
@@ -104,6 +109,9 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     const int pair = tid / kFoldTPR, part = tid % kFoldTPR;
     long long item_base = 0;  // items enumerated in earlier scan passes
     uint32_t phase = 0;
+    // set when a drain wait ran out too: copies may still land in the buffers,
+    // so the CTA only marks the rows of its remaining items as failed
+    bool dead = false;
 
     if (tid == 0) {
         ptx::mbar_init(bar, 1);
@@ -164,6 +172,10 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const float *ring_g = FL.ring_g[li];
             const float *ring_beta = FL.ring_beta[li];
             float *ckpt = FL.checkpoint[li];
+            if (dead) {
+                if (tid == 0) C.is_flush[slot_e] = kFoldFailed;
+                continue;
+            }
 
             // ---- 1. keys and values by bulk copies (warp 0): the keys are one
             //         or two contiguous ring segments, the values one run of
@@ -220,14 +232,21 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                 }
             }
             // ---- 3. the copies land; 1 / |k_t| for every record (two threads each)
-            const bool landed = ptx::mbar_wait(bar, phase);
+            const bool landed = ptx::mbar_wait(bar, phase, wait_limit);
             phase ^= 1u;
             if (__syncthreads_or(!landed)) {   // the same decision in every thread
-                // record the failure, give the copies one more bounded wait so
-                // that none is still writing this CTA's shared memory, and stop
-                if (tid == 0) atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
-                ptx::mbar_wait(bar, phase ^ 1u);
-                return;
+                // record the failure and mark the row (its other items may be
+                // folded already: the cursor move poisons it), give the copies
+                // one more bounded wait so that none is still writing this
+                // CTA's shared memory, and go on with the next item.  The flag
+                // stays non-zero, so every CTA still builds the same slot list.
+                if (tid == 0) {
+                    atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
+                    C.is_flush[slot_e] = kFoldFailed;
+                }
+                const bool drained = ptx::mbar_wait(bar, phase ^ 1u, kWaitLimitDefault);
+                if (__syncthreads_or(!drained)) dead = true;
+                continue;
             }
             // (the trip count is the same in every thread: the shuffle is warp-wide)
             for (int j0 = 0; j0 < W; j0 += kFoldThreads / 2) {
@@ -357,7 +376,7 @@ static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n
     if (e != cudaSuccess) return e;
     // enough CTAs for every item of a typical step to run at once; the ones
     // without an item leave after the flag scan
-    kern<<<4 * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B);
+    kern<<<4 * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B, data_wait_limit());
     return cudaGetLastError();
 }
 

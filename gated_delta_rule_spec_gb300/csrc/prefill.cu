@@ -79,7 +79,7 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
                const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
                const IO *__restrict__ a, const IO *__restrict__ bgate, const float *__restrict__ A_log,
                const float *__restrict__ dt_bias, IO *__restrict__ out, int from_zero,
-               float *__restrict__ snap) {
+               float *__restrict__ snap, uint32_t wait_limit) {
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
     constexpr int kPer = KC::kVals;                 // values per 16-byte chunk
@@ -192,13 +192,18 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
                 }
             }
             // ---- 3. the copies land; 1/|k_t| and 1/|q_t| (two threads per token)
-            const bool landed = ptx::mbar_wait(bar, phase);
+            const bool landed = ptx::mbar_wait(bar, phase, wait_limit);
             phase ^= 1u;
             if (__syncthreads_or(!landed)) {   // the same decision in every thread
-                // record the failure, give the copies one more bounded wait so
-                // that none is still writing this CTA's shared memory, and stop
-                if (tid == 0) atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
-                ptx::mbar_wait(bar, phase ^ 1u);
+                // record the failure (and, for prefill, mark the row so that its
+                // cursor reset poisons it instead), give the copies one more
+                // bounded wait so that none is still writing this CTA's shared
+                // memory, and stop
+                if (tid == 0) {
+                    atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
+                    if (!SNAP) C.is_flush[slot] = kFoldFailed;
+                }
+                ptx::mbar_wait(bar, phase ^ 1u, kWaitLimitDefault);
                 failed = true;
                 break;
             }
@@ -378,13 +383,20 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
     }
 }
 
-// After the prefill: the cursors of the rows it computed are reset for decode.
+// After the prefill: the cursors of the rows it computed are reset for decode;
+// a row whose prefill stopped on a wait that ran out (marked kFoldFailed) is
+// poisoned instead (write_pos = -1: CURSOR_CORRUPT until gdn_spec_reset).
 __global__ void prefill_cursor_kernel(CursorArgs C, int L, const int32_t *__restrict__ slot_idx, int B,
                                       int from_zero) {
     for (int bb = blockIdx.x * blockDim.x + threadIdx.x; bb < B; bb += gridDim.x * blockDim.x) {
         const int slot = slot_idx[bb];
         uint32_t st;
         if (!prefill_row_ok(C, slot, L, from_zero, &st)) continue;
+        if (C.is_flush[slot] == kFoldFailed) {
+            C.write_pos[slot] = -1;
+            C.is_flush[slot] = 0;
+            continue;
+        }
         C.write_pos[slot] = 0;
         C.cache_base[slot] = 0;
         C.is_flush[slot] = 0;
@@ -436,7 +448,7 @@ static cudaError_t launch_prefill_k(const LayerArgs &P, const CursorArgs &C, con
         kern<<<grid, kPreThreads, smem, stream>>>(
             P, C, slot_idx, B, N, static_cast<const IO *>(q), static_cast<const IO *>(k),
             static_cast<const IO *>(v), static_cast<const IO *>(a), static_cast<const IO *>(b), A_log,
-            dt_bias, static_cast<IO *>(out), from_zero, snap);
+            dt_bias, static_cast<IO *>(out), from_zero, snap, data_wait_limit());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (SNAP) return cudaSuccess;
     const int cb = (B + 255) / 256;

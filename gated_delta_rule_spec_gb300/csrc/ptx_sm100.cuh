@@ -44,9 +44,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
-// Bounded wait on phase `parity`; false if the limit ran out (~0.3 s).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < (1u << 20); ++it) {
+// Bounded wait on phase `parity`; false if `limit` polls ran out (the
+// default, 2^20 polls, is about 0.3 s).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = 1u << 20) {
+    for (uint32_t it = 0; it < limit; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (it > 32) __nanosleep(256);
     }

@@ -36,6 +36,8 @@
 // which no CTA reads in this launch.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx_sm100.cuh"
 
@@ -256,7 +258,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                  const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                  const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ a,
                  const __nv_bfloat16 *__restrict__ bgate, const float *__restrict__ A_log,
-                 const float *__restrict__ dt_bias, __nv_bfloat16 *__restrict__ out) {
+                 const float *__restrict__ dt_bias, __nv_bfloat16 *__restrict__ out,
+                 uint32_t tile_wait_limit) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = ptx::smem_addr(smem_raw);
     const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
@@ -721,7 +724,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                                  dt_bias, R);
         }
         if (ok) {
-            waited = ptx::mbar_wait(bar_s0, ph_s0);
+            waited = ptx::mbar_wait(bar_s0, ph_s0, tile_wait_limit);
             ph_s0 ^= 1u;
             if (!waited) lost |= 4u;
             if (tid == 0) {
@@ -803,55 +806,121 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 
 EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static std::once_flag once;
+    std::call_once(once, [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                              &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+    });
     return fn;
 }
 
+// Per-device launch set-up, done once per device and kernel instance: the
+// shared-memory attributes and the grid size.  The grid comes from the
+// resources themselves (shared memory with the per-CTA reserve, and
+// kCtasPerSm): the runtime's occupancy query answers 1 for this kernel
+// whatever the sizes, yet the SM holds three of its CTAs (measured: all
+// 3 x SMs CTAs of one launch start within a few microseconds), and one per SM
+// would leave two thirds of the machine idle.
+constexpr int kMaxDevices = 64;
+struct DeviceSetup {
+    bool done[2];
+    int grid_cap;
+};
+DeviceSetup g_setup[kMaxDevices];
+std::mutex g_setup_mu;
+
 template <int TM>
-cudaError_t launch_tm(const CUtensorMap &tmap, const LayerArgs &P, const CursorArgs &C,
+cudaError_t device_setup(int dev, int slot_tm, int *grid_cap) {
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    DeviceSetup &d = g_setup[dev];
+    if (!d.done[slot_tm]) {
+        auto kern = tc::verify_tc_kernel<TM>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             tc::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        // all of the unified L1 / shared storage as shared memory
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        int sms = 0, smem_sm = 0, smem_rsv = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+            cudaSuccess)
+            return e;
+        int per_sm = smem_sm / (tc::kSmemBytes + smem_rsv);
+        if (per_sm > tc::kCtasPerSm) per_sm = tc::kCtasPerSm;
+        if (per_sm < 1) per_sm = 1;
+        d.grid_cap = sms * per_sm;
+        d.done[slot_tm] = true;
+    }
+    *grid_cap = d.grid_cap;
+    return cudaSuccess;
+}
+
+// The checkpoint as a 2-D tensor [num_slots * HV * V rows, K fp32], boxes of
+// 32 x 128 (one 128-byte swizzle span by the CTA's 128 rows).  The map
+// depends only on the checkpoint's address and row count, so the last few
+// are kept.
+constexpr int kMapCache = 16;
+struct MapEntry {
+    const float *ptr;
+    uint64_t rows;
+    int dev;
+    CUtensorMap map;
+};
+MapEntry g_maps[kMapCache];
+int g_maps_used = 0, g_maps_next = 0;
+std::mutex g_maps_mu;
+
+bool tensor_map(const LayerArgs &P, int dev, CUtensorMap *out) {
+    const uint64_t rows = (uint64_t)P.num_slots * P.HV * P.V;
+    std::lock_guard<std::mutex> lk(g_maps_mu);
+    for (int i = 0; i < g_maps_used; ++i)
+        if (g_maps[i].ptr == P.checkpoint && g_maps[i].rows == rows && g_maps[i].dev == dev) {
+            *out = g_maps[i].map;
+            return true;
+        }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    CUtensorMap tmap;
+    const cuuint64_t gdim[2] = {(cuuint64_t)P.K, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)P.K * sizeof(float)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)tc::kBV};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.checkpoint, gdim, gstride, box,
+                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    MapEntry &e = g_maps[g_maps_next];
+    e.ptr = P.checkpoint;
+    e.rows = rows;
+    e.dev = dev;
+    e.map = tmap;
+    g_maps_next = (g_maps_next + 1) % kMapCache;
+    if (g_maps_used < kMapCache) ++g_maps_used;
+    *out = tmap;
+    return true;
+}
+
+template <int TM>
+cudaError_t launch_tm(const CUtensorMap &tmap, int grid_cap, const LayerArgs &P, const CursorArgs &C,
                       const int32_t *slot_idx, int B, const void *q, const void *k, const void *v,
                       const void *a, const void *b, const float *A_log, const float *dt_bias,
                       void *out, cudaStream_t stream) {
-    auto kern = tc::verify_tc_kernel<TM>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // all of the unified L1 / shared storage as shared memory
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    // CTAs per SM from the resources themselves: shared memory (with the
-    // per-CTA reserve) and kCtasPerSm.  The runtime's occupancy query answers 1
-    // for this kernel whatever the sizes, yet the SM holds three of its CTAs
-    // (measured: all 3 x SMs CTAs of one launch start within a few
-    // microseconds), and one per SM would leave two thirds of the machine idle.
-    int dev = 0, sms = 0, smem_sm = 0, smem_rsv = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
-        cudaSuccess)
-        return e;
-    if ((e = cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
-        cudaSuccess)
-        return e;
-    int per_sm = smem_sm / (tc::kSmemBytes + smem_rsv);
-    if (per_sm > tc::kCtasPerSm) per_sm = tc::kCtasPerSm;
-    if (per_sm < 1) per_sm = 1;
     const int nunits = B * P.HV * (P.V / tc::kBV);
-    int grid = sms * per_sm;
-    if (grid > nunits) grid = nunits;
-    kern<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(
+    const int grid = grid_cap < nunits ? grid_cap : nunits;
+    tc::verify_tc_kernel<TM><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(
         tmap, P, C, slot_idx, nunits, static_cast<const __nv_bfloat16 *>(q),
         static_cast<const __nv_bfloat16 *>(k), static_cast<const __nv_bfloat16 *>(v),
         static_cast<const __nv_bfloat16 *>(a), static_cast<const __nv_bfloat16 *>(b), A_log, dt_bias,
-        static_cast<__nv_bfloat16 *>(out));
+        static_cast<__nv_bfloat16 *>(out), data_wait_limit());
     return cudaGetLastError();
 }
 
@@ -861,22 +930,19 @@ cudaError_t launch_verify_tc(const LayerArgs &P, const CursorArgs &C, const int3
                              int B, const void *q, const void *k, const void *v, const void *a,
                              const void *b, const float *A_log, const float *dt_bias, void *out,
                              cudaStream_t stream) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    // the checkpoint as a 2-D tensor [num_slots * HV * V rows, K fp32], boxes of
-    // 32 x 128 (one 128-byte swizzle span by the CTA's 128 rows)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {(cuuint64_t)P.K, (cuuint64_t)P.num_slots * P.HV * P.V};
-    const cuuint64_t gstride[1] = {(cuuint64_t)P.K * sizeof(float)};
-    const cuuint32_t box[2] = {32, (cuuint32_t)tc::kBV};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, P.checkpoint, gdim, gstride, box,
-                     estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (P.T <= 4)
-        return launch_tm<4>(tmap, P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, stream);
-    return launch_tm<8>(tmap, P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, stream);
+    if (!tensor_map(P, dev, &tmap)) return cudaErrorInvalidValue;
+    int grid_cap = 0;
+    if (P.T <= 4) {
+        if ((e = device_setup<4>(dev, 0, &grid_cap)) != cudaSuccess) return e;
+        return launch_tm<4>(tmap, grid_cap, P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, stream);
+    }
+    if ((e = device_setup<8>(dev, 1, &grid_cap)) != cudaSuccess) return e;
+    return launch_tm<8>(tmap, grid_cap, P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, stream);
 }
 
 }  // namespace gdnspec

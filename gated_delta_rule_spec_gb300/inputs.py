@@ -126,11 +126,23 @@ def layer_params(rng: np.random.Generator, HV: int, K: int, per_key_gate: bool):
     return A_log, dt_bias
 
 
+def _row_scales(rng: np.random.Generator, shape, scale_range):
+    """Per-row factors drawn log-uniformly from scale_range (lo, hi), shape + (1,)."""
+    lo, hi = scale_range
+    f = np.exp(rng.uniform(np.log(lo), np.log(hi), size=shape))
+    return f.astype(np.float32)[..., None]
+
+
 def window_inputs(rng: np.random.Generator, B: int, T: int, H: int, HV: int, K: int, V: int,
-                  io_dtype: str, per_key_gate: bool = False):
-    """q, k, v, a, b ~ N(0, 1) with q, k scaled to unit norm per (token, head)."""
+                  io_dtype: str, per_key_gate: bool = False, key_scale=None):
+    """q, k, v, a, b ~ N(0, 1) with q, k scaled to unit norm per (token, head).
+    key_scale=(lo, hi): q and k rows are then multiplied by factors drawn
+    log-uniformly from [lo, hi] (raw, non-unit inputs)."""
     q = _unit_rows(rng.standard_normal((B, T, H, K), dtype=np.float32))
     k = _unit_rows(rng.standard_normal((B, T, H, K), dtype=np.float32))
+    if key_scale is not None:
+        q = q * _row_scales(rng, (B, T, H), key_scale)
+        k = k * _row_scales(rng, (B, T, H), key_scale)
     v = rng.standard_normal((B, T, HV, V), dtype=np.float32)
     a_shape = (B, T, HV, K) if per_key_gate else (B, T, HV)
     a = rng.standard_normal(a_shape, dtype=np.float32)
@@ -140,10 +152,14 @@ def window_inputs(rng: np.random.Generator, B: int, T: int, H: int, HV: int, K: 
 
 
 def token_stream(rng: np.random.Generator, n: int, H: int, HV: int, K: int, V: int,
-                 io_dtype: str, per_key_gate: bool = False):
+                 io_dtype: str, per_key_gate: bool = False, key_scale=None):
     """Raw per-token records for a run of n tokens of one batch row:
-    k [n, H, K] (unit norm), v [n, HV, V], a [n, HV] (KDA [n, HV, K]), b [n, HV]."""
+    k [n, H, K] (unit norm; with key_scale=(lo, hi) each row then multiplied by a
+    factor drawn log-uniformly from [lo, hi]), v [n, HV, V], a [n, HV] (KDA
+    [n, HV, K]), b [n, HV]."""
     k = _unit_rows(rng.standard_normal((n, H, K), dtype=np.float32))
+    if key_scale is not None:
+        k = k * _row_scales(rng, (n, H), key_scale)
     v = rng.standard_normal((n, HV, V), dtype=np.float32)
     a = rng.standard_normal((n, HV, K) if per_key_gate else (n, HV), dtype=np.float32)
     b = rng.standard_normal((n, HV), dtype=np.float32)

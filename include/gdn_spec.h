@@ -66,7 +66,9 @@
 extern "C" {
 #endif
 
-#define GDN_SPEC_ABI_VERSION 2   /* 2: adds gdn_spec_prefill and the snapshot comparison calls */
+#define GDN_SPEC_ABI_VERSION 3   /* 2: adds gdn_spec_prefill and the snapshot comparison calls;
+                                    3: adds gdn_spec_set_wait_limit, commit's cursor check and the
+                                       poisoning of rows a fold or prefill could not finish */
 
 /* host-side error codes (return values) */
 #define GDN_SPEC_OK            0
@@ -81,9 +83,15 @@ extern "C" {
 #define GDN_SPEC_ST_SLOT_OOR       2u  /* slot_idx[b] >= num_slots                        */
 #define GDN_SPEC_ST_RING_OVERFLOW  4u  /* verify: write_pos + T > L (a fold was skipped)  */
 #define GDN_SPEC_ST_CURSOR_CORRUPT 8u  /* write_pos < 0, write_pos > L or cache_base outside [0, L) */
-#define GDN_SPEC_ST_TIMEOUT       16u  /* a bounded device wait ran out: that call's outputs are invalid
-                                              (the CTA that saw it drains its copies and stops, so rows it
-                                              had not reached keep whatever `out` held) */
+#define GDN_SPEC_ST_TIMEOUT       16u  /* a bounded device wait ran out: that call's outputs are invalid.
+                                              verify: the CTA that saw it drains its copies and stops, so
+                                              rows it had not reached keep whatever `out` held and their
+                                              window records may be missing from the ring (do not commit
+                                              that step).  fold / prefill: every row with an unfinished
+                                              item is poisoned (write_pos = -1, so later calls report
+                                              CURSOR_CORRUPT for it); its checkpoint may be partly folded
+                                              or partly prefilled, so the slot must be rebuilt:
+                                              gdn_spec_reset, then gdn_spec_prefill. */
 #define GDN_SPEC_ST_UNFOLDED      32u  /* prefill: continuing from a checkpoint whose ring is not folded */
 
 #define GDN_SPEC_GATE_SCALAR  0    /* GDN: one gate per (token, v-head)            */
@@ -160,6 +168,8 @@ int gdn_spec_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors
  * are overwritten by the next verify ([blog] §4.2-4.3).
  *   accept_len  int32 [B], device; 0 <= accept_len <= T (it counts the bonus
  *               token); outside that the row is skipped with ACCEPT_RANGE.
+ * A row whose cursors are out of range (write_pos outside [0, L], cache_base
+ * outside [0, L)) is skipped with CURSOR_CORRUPT and left as it is.
  */
 int gdn_spec_commit(const gdn_spec_cursors *cursors, int32_t T, int32_t L,
                     const int32_t *slot_idx, int32_t B, const int32_t *accept_len,
@@ -241,6 +251,19 @@ int gdn_spec_snapshot_verify(const gdn_spec_layer *layer, const gdn_spec_cursors
 int gdn_spec_snapshot_commit(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,
                              const int32_t *slot_idx, int32_t B, const int32_t *accept_len,
                              const float *snap, void *stream);
+
+/*
+ * gdn_spec_set_wait_limit -- diagnostic: the number of polls after which the
+ * first wait on each asynchronous data copy gives up (verify's checkpoint
+ * tile on the tensor-core path, the fold's ring records, prefill's prompt
+ * chunks).  A wait that gives up sets GDN_SPEC_ST_TIMEOUT; the copy is then
+ * drained with the default limit before its buffer is reused, so a small
+ * limit exercises the timeout path without leaving anything in flight.
+ * Applies to calls made (or graphs captured) afterwards, in every thread of
+ * the process.  0xFFFFFFFF restores the default (2^20 polls, about 0.3 s).
+ * Returns the previous limit.  Not for production use.
+ */
+uint32_t gdn_spec_set_wait_limit(uint32_t polls);
 
 /*
  * gdn_spec_read_status -- copy the device status word to *host_out after

@@ -48,7 +48,13 @@ class Scenario:
 
     def __init__(self, wl: gen.Workload, B: int, seed: int = 0, num_slots: int | None = None,
                  slot_idx: np.ndarray | None = None, random_cursors: bool = False,
-                 prefix: int | None = None, decay_shift: float = 0.0, scale: float = 1.0):
+                 prefix: int | None = None, decay_shift: float = 0.0, scale: float = 1.0,
+                 key_scale=None, cursors=None):
+        """key_scale=(lo, hi): every key (prefix, ring history, window) and query
+        row is scaled by a factor drawn log-uniformly from [lo, hi], so the
+        kernels' in-kernel L2 norms see non-unit inputs.  cursors=(write_pos,
+        cache_base, is_flush): start from these cursor arrays (the ring history
+        is filled at their positions), e.g. to share one set between layers."""
         self.wl = wl
         self.B = B
         self.num_slots = num_slots or (B + 1)
@@ -60,6 +66,7 @@ class Scenario:
         self.io = wl.io_dtype
         self.G = wl.HV // wl.H
         self.decay_shift = decay_shift   # subtracted from a: weaker decays
+        self.key_scale = key_scale
         self.A_log, self.dt_bias = gen.layer_params(r, d.HV, d.K, d.per_key_gate)
         if slot_idx is None:
             slot_idx = (gen.scattered_slots(r, self.num_slots, B) if self.num_slots > B
@@ -69,7 +76,9 @@ class Scenario:
 
         ring = gen.garbage_ring(r, d.num_slots, d.H, d.HV, d.L, d.K, d.V, self.io, d.per_key_gate)
         ckpt = (r.standard_normal((d.num_slots, d.HV, d.V, d.K), dtype=np.float32) * 0.1)
-        if random_cursors:
+        if cursors is not None:
+            wp, base, flag = (np.asarray(c, np.int32).copy() for c in cursors)
+        elif random_cursors:
             wp, base, flag = gen.random_cursors(r, d.num_slots, d.L, d.T)
         else:
             wp = np.zeros(d.num_slots, np.int32)
@@ -78,7 +87,7 @@ class Scenario:
         pre = wl.prefix if prefix is None else prefix
         if used and pre > 0:
             ckpt[used] = self._prefix_states(used, pre).astype(np.float32)
-        if random_cursors and used:
+        if (random_cursors or cursors is not None) and used:
             self._fill_history(ring, used, wp, base)
         self.ring0 = {k2: v2.copy() for k2, v2 in ring.items()}
 
@@ -111,7 +120,7 @@ class Scenario:
     def _token_records(self, n_units_rows: int, n: int):
         d = self.dims
         st = gen.token_stream(self.rng, n * n_units_rows, d.H, d.HV, d.K, d.V, self.io,
-                              d.per_key_gate)
+                              d.per_key_gate, key_scale=self.key_scale)
         k = st["k"].reshape(n_units_rows, n, d.H, d.K)
         v = st["v"].reshape(n_units_rows, n, d.HV, d.V)
         a = st["a"].reshape((n_units_rows, n, d.HV) + ((d.K,) if d.per_key_gate else ()))
@@ -153,7 +162,8 @@ class Scenario:
 
     def window(self):
         d = self.dims
-        w = gen.window_inputs(self.rng, self.B, d.T, d.H, d.HV, d.K, d.V, self.io, d.per_key_gate)
+        w = gen.window_inputs(self.rng, self.B, d.T, d.H, d.HV, d.K, d.V, self.io, d.per_key_gate,
+                              key_scale=self.key_scale)
         if self.decay_shift:
             a = gen.to_f64(w["a"]).astype(np.float32) - np.float32(self.decay_shift)
             w["a"] = gen.store(a, self.io)
@@ -215,6 +225,16 @@ class Scenario:
             got, want = got[slots], want[slots]
         den = np.linalg.norm(want)
         return float(np.linalg.norm(got - want) / den) if den > 0 else float(np.linalg.norm(got))
+
+    def ckpt_error_per_slot(self, slots) -> float:
+        """Largest relative Frobenius error of one (slot, v-head) checkpoint among
+        the given slots (a stray write into one state is not diluted by the rest)."""
+        got = to_host(self.layer.checkpoint).astype(np.float64)[slots]
+        want = self.orc.checkpoint[slots]
+        num = np.linalg.norm((got - want).reshape(got.shape[0], got.shape[1], -1), axis=-1)
+        den = np.linalg.norm(want.reshape(want.shape[0], want.shape[1], -1), axis=-1)
+        rel = np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+        return float(rel.max()) if rel.size else 0.0
 
     def out_tol(self) -> float:
         return OUT_TOL_BF16 if self.io == gen.BF16 else OUT_TOL_FP32

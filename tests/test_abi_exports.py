@@ -72,3 +72,11 @@ def test_descriptor_layout_matches_header():
     assert ctypes.sizeof(binding.LayerDesc) == 9 * 4 + 2 * 4 + 4 + 5 * 8  # 4 bytes padding
     assert binding.LayerDesc.checkpoint.offset == 48
     assert ctypes.sizeof(binding.CursorDesc) == 8 + 4 * 8
+
+
+def test_wait_limit_setter_is_host_only_and_restores_the_default(lib):
+    """gdn_spec_set_wait_limit only records a number on the host (no CUDA call):
+    it returns the previous limit, and 0xFFFFFFFF restores the default 2^20."""
+    assert binding.set_wait_limit(7) == 1 << 20
+    assert binding.set_wait_limit(binding.WAIT_LIMIT_DEFAULT) == 7
+    assert binding.set_wait_limit(binding.WAIT_LIMIT_DEFAULT) == 1 << 20

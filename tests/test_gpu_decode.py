@@ -34,7 +34,7 @@ def _decode_rounds(sc, rounds, ring_every):
         folds += int(sc.orc_cur.is_flush[sc.slot_idx].sum())
         assert sc.fold() == 0
         sc.check_cursors()
-        assert sc.ckpt_error(slots=sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
+        assert sc.ckpt_error_per_slot(sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
     assert binding.read_status(sc.cur) == 0
     return worst, folds
 

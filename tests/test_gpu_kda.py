@@ -27,7 +27,7 @@ def _kda_rounds(sc, rounds, ring_every):
         assert sc.commit(acc) == 0
         assert sc.fold() == 0
         sc.check_cursors()
-        assert sc.ckpt_error(slots=sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
+        assert sc.ckpt_error_per_slot(sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
     assert binding.read_status(sc.cur) == 0
     return worst
 

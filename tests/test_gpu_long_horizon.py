@@ -58,7 +58,7 @@ def test_c3_flush_heavy_16k_tokens():
         if committed[TRACKED[0]] >= next_log:
             next_log += log_every
             e_out = sc.out_error(out, o_orc, rows=list(TRACKED))
-            e_ck = sc.ckpt_error(slots=list(tracked_slots))
+            e_ck = sc.ckpt_error_per_slot(list(tracked_slots))
             for name in ("write_pos", "cache_base", "is_flush"):
                 got = to_host(getattr(sc.cur, name))[tracked_slots]
                 assert np.array_equal(got, getattr(sc.orc_cur, name)[tracked_slots]), name

@@ -34,7 +34,7 @@ def _rounds(sc: Scenario, rounds: int, full_frac: float = 0.0, check_ring_every:
         sc.check_cursors()
         assert sc.fold() == 0
         sc.check_cursors()
-        e = sc.ckpt_error(slots=sorted(set(sc.slot_idx.tolist())))
+        e = sc.ckpt_error_per_slot(sorted(set(int(x) for x in sc.slot_idx if x >= 0)))
         worst["ckpt"] = max(worst["ckpt"], e)
         assert e <= CKPT_REL_FRO, f"round {r}: checkpoint error {e}"
     assert binding.read_status(sc.cur) == 0
@@ -102,7 +102,11 @@ def test_c2_batch_sweep_scattered_slots(B):
     assert sc.commit(acc) == 0
     assert sc.fold() == 0
     sc.check_cursors()
-    assert sc.ckpt_error() <= CKPT_REL_FRO
+    # every (slot, v-head) of the batch on its own, and every other slot bitwise
+    assert sc.ckpt_error_per_slot(sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
+    others = sorted(set(range(sc.num_slots)) - set(sc.slot_idx.tolist()))
+    assert np.array_equal(to_host(sc.layer.checkpoint)[others],
+                          sc.orc.checkpoint[others].astype(np.float32))
     # a second round on the moved cursors
     w = sc.window()
     out, o_orc, st = sc.verify(w)

@@ -56,7 +56,7 @@ def test_tc_fold_deferred_until_the_ring_is_full():
         sc.check_cursors()
     assert sc.fold() == 0
     sc.check_cursors()
-    assert sc.ckpt_error(slots=sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
+    assert sc.ckpt_error_per_slot(sorted(set(sc.slot_idx.tolist()))) <= CKPT_REL_FRO
     out, o_orc, st = sc.verify(sc.window())
     assert st == 0 and sc.out_error(out, o_orc) <= sc.out_tol()
     assert binding.read_status(sc.cur) == 0
