@@ -209,7 +209,11 @@ class Workload:
 
 def build_state(wl: Workload, seed: int, device, random_rounds: int = 48):
     """Layer state built by the library's own rounds from a zero checkpoint:
-    16 full-accept rounds, then random_rounds with accept_len ~ U{1..T}."""
+    16 full-accept rounds, then random_rounds with accept_len ~ U{1..T}.  During
+    the random rounds each row first sits out a random number of rounds (accept
+    0), drawn from [0, one fold cycle] (a cycle is about (L - 2T) / E[accept_len]
+    rounds), so that the rows' ring fill levels and fold times spread out as in
+    a serving batch instead of moving in lockstep."""
     import torch
     from gated_delta_rule_spec_gb300 import binding
     from gated_delta_rule_spec_gb300 import inputs as gen
@@ -230,10 +234,17 @@ def build_state(wl: Workload, seed: int, device, random_rounds: int = 48):
 
     binding.reset(cur, slots)
     full = torch.full((wl.B,), wl.T, dtype=torch.int32, device=device)
+    cycle = (wl.L - 2 * wl.T) * 2 // (wl.T + 1) + 2
+    pause = rng.integers(0, max(1, cycle), size=wl.B)
     for r in range(16 + random_rounds):
         w = dev_window()
         binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias)
-        acc = full if r < 16 else torch.from_numpy(gen.accept_lens(rng, wl.B, wl.T)).to(device)
+        if r < 16:
+            acc = full
+        else:
+            a_np = gen.accept_lens(rng, wl.B, wl.T)
+            a_np[pause > r - 16] = 0
+            acc = torch.from_numpy(a_np).to(device)
         binding.commit(cur, wl.T, wl.L, slots, acc)
         binding.fold(layer, cur, slots)
     torch.cuda.synchronize()

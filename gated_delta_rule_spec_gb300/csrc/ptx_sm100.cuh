@@ -1,8 +1,8 @@
 // ptx_sm100.cuh -- thin inline-PTX wrappers for the Blackwell (sm_100 family,
 // built here for sm_103a) features the tensor-core verify kernel uses:
 // mbarriers, TMA tile loads and L2 bulk prefetch, and the 5th-generation
-// tensor core (tcgen05: TMEM allocation, MMA with an fp32 TMEM accumulator,
-// commit to an mbarrier, TMEM -> register loads).
+// tensor core (tcgen05: TMEM allocation, tf32 and bf16 MMAs with an fp32 TMEM
+// accumulator, commit to an mbarrier, TMEM -> register loads).
 //
 // Every wait here is bounded: a wait that runs out returns false, and the
 // caller records a status bit instead of spinning forever.
@@ -138,6 +138,27 @@ __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
            | ((M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor of kind::f16 with bf16 A and B: fp32 accumulator,
+// both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+    return (1u << 4)            // D format: f32
+           | (1u << 7)          // A format: bf16
+           | (1u << 10)         // B format: bf16
+           | ((N >> 3) << 17)   // N / 8
+           | ((M >> 4) << 24);  // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one MMA of K = 16 bf16 elements.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, one MMA of K = 8 tf32 elements.
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -168,6 +189,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
+}
+
+// Warp-wide: 8 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8]) {
+    uint32_t u[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = __uint_as_float(u[i]);
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

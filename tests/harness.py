@@ -151,7 +151,8 @@ class Scenario:
         n = d.L
         k, v, g, beta = self._token_records(len(used), n)
         for i, slot in enumerate(used):
-            for o in range(int(wp[slot])):
+            # (a corrupt write_pos outside [0, L] gets no records beyond the ring)
+            for o in range(max(0, min(int(wp[slot]), d.L))):
                 p = (int(base[slot]) + o) & (d.L - 1)
                 ring["rawk"][slot, :, p] = k[i, o]
                 ring["rawv"][slot, :, p] = v[i, o]

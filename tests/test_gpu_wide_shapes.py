@@ -80,3 +80,13 @@ def test_kda_window_of_eight_tokens():
     sc = Scenario(wl, B=2, seed=13, num_slots=3, decay_shift=2.0)
     assert binding.verify_path(sc.layer) == "generic"
     _kda_rounds(sc, 15, ring_every=3)
+
+
+@pytest.mark.parametrize("H,HV", [(4, 4), (2, 6)])
+def test_tc_single_head_units_odd_groups(H, HV):
+    """An odd number of v-heads per q/k head (G = 1, G = 3): the tensor-core
+    kernel takes one v-head per unit instead of a pair."""
+    wl = gen.Workload(f"tc-g{HV // H}", B=3, H=H, HV=HV, K=128, V=128, T=4, L=16, prefix=16)
+    sc = Scenario(wl, B=3, seed=51 + HV, num_slots=5, decay_shift=2.0, random_cursors=True)
+    assert binding.verify_path(sc.layer) == "tc"
+    _rounds(sc, 16, full_frac=0.3, check_ring_every=2)
