@@ -9,8 +9,9 @@
 //     d  = beta_t (v_t - S k^_t),   S <- S + d k^_t^T
 //
 // Rows of S are independent under the recurrence (row i only sees v_t[i]).
-// A thread owns one quarter of the K columns of TWO state rows (rows p and
-// p + 32 of a 64-row block; a row's dot product takes two shuffles), so
+// A thread owns an eighth of the K columns of TWO state rows (rows p and
+// p + 16 of a 32-row block; a row's dot product takes three shuffles; at
+// K = 32 a quarter of the columns of rows p and p + 32 of a 64-row block), so
 // every key value it reads from shared memory serves both rows.  The keys
 // stay in shared memory as the raw I/O-dtype records (bf16: half the bytes
 // of fp32) and are widened in registers: reading the keys is what bounds the
@@ -50,11 +51,20 @@
 namespace gdnspec {
 
 constexpr int kFoldThreads = 128;
-constexpr int kFoldTPR = 4;                           // threads per pair of state rows
-constexpr int kFoldPairs = kFoldThreads / kFoldTPR;   // 32
-constexpr int kFoldRows = 2 * kFoldPairs;             // state rows per work item
 constexpr int kFoldMaxL = 128;                        // ring length limit of this kernel
 constexpr int kFoldScan = kFoldThreads;
+
+// Threads per pair of state rows: eight at K >= 64 (a pair's dot products
+// take three shuffles; 32 state rows per work item), four at K = 32 (two
+// shuffles; 64 rows per item).  Eight gives twice the items, which spreads a
+// step's few flagged rows over more SMs and more warps per SM.
+template <int K>
+struct FoldGeom {
+    static constexpr int TPR = K >= 64 ? 8 : 4;
+    static constexpr int Pairs = kFoldThreads / TPR;
+    static constexpr int Rows = 2 * Pairs;            // state rows per work item
+    static constexpr int CtasPerSm = K >= 64 ? 6 : 4;
+};
 
 __host__ __device__ constexpr size_t fold_pad16(size_t bytes) { return (bytes + 15) & ~(size_t)15; }
 
@@ -65,9 +75,10 @@ __host__ __device__ constexpr size_t fold_pad16(size_t bytes) { return (bytes + 
 struct FoldSmem {
     size_t keys, vals, alpha, beta, rs, rows, meta, total;
     __host__ __device__ FoldSmem(int K, int L, bool kda, size_t io) {
+        const int item_rows = K >= 64 ? FoldGeom<128>::Rows : FoldGeom<32>::Rows;
         keys = 0;
         vals = keys + fold_pad16((size_t)L * K * io);
-        alpha = vals + fold_pad16((size_t)L * kFoldRows * io);
+        alpha = vals + fold_pad16((size_t)L * item_rows * io);
         beta = alpha + fold_pad16(sizeof(float) * (size_t)L * (kda ? K : 2));
         rs = beta + fold_pad16(sizeof(float) * L);
         rows = rs + fold_pad16(sizeof(float) * L);
@@ -81,13 +92,16 @@ size_t fold_smem_bytes(int K, int L, bool kda, bool bf16) {
 }
 
 template <typename IO, bool KDA, int K>
-__global__ void __launch_bounds__(kFoldThreads, 4)
+__global__ void __launch_bounds__(kFoldThreads, FoldGeom<K>::CtasPerSm)
 fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int32_t *__restrict__ slot_idx, int B, uint32_t wait_limit) {
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
+    constexpr int kFoldTPR = FoldGeom<K>::TPR;
+    constexpr int kFoldPairs = FoldGeom<K>::Pairs;
+    constexpr int kFoldRows = FoldGeom<K>::Rows;
     constexpr int kPer = KC::kVals;                 // key values per 16-byte chunk
-    constexpr int kNC = K / kPer / kFoldTPR;        // chunks per thread: chunk part + 4 m
+    constexpr int kNC = K / kPer / kFoldTPR;        // chunks per thread: chunk part + TPR m
     constexpr int kNP = kNC * kPer / 2;             // float2 pairs per thread and row
     static_assert(kNC >= 1, "at least one chunk per thread");
     extern __shared__ __align__(16) uint8_t smem[];
@@ -221,7 +235,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                     const float *srow = ckpt + (sh_hv * V + row0 + pair + rr * kFoldPairs) * K;
 #pragma unroll
                     for (int m = 0; m < kNC; ++m) {
-                        const float4 *src = reinterpret_cast<const float4 *>(srow + (part + 4 * m) * kPer);
+                        const float4 *src = reinterpret_cast<const float4 *>(srow + (part + kFoldTPR * m) * kPer);
 #pragma unroll
                         for (int q = 0; q < kPer / 4; ++q) {
                             const float4 f = src[q];
@@ -276,7 +290,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
 #pragma unroll
                 for (int m = 0; m < kNC; ++m) {
                     float2 c2[kPer / 2];
-                    KC::widen(xk[part + 4 * m], c2);
+                    KC::widen(xk[part + kFoldTPR * m], c2);
 #pragma unroll
                     for (int i = 0; i < kPer / 2; ++i) x[m * (kPer / 2) + i] = c2[i];
                 }
@@ -284,7 +298,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                     const float *al = alpha + (size_t)t * K;
 #pragma unroll
                     for (int m = 0; m < kNC; ++m) {
-                        const float4 *a4 = reinterpret_cast<const float4 *>(al + (part + 4 * m) * kPer);
+                        const float4 *a4 = reinterpret_cast<const float4 *>(al + (part + kFoldTPR * m) * kPer);
 #pragma unroll
                         for (int q = 0; q < kPer / 4; ++q) {
                             const float4 a = a4[q];
@@ -320,10 +334,11 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                 }
                 float u0 = (acc[0][0].x + acc[0][0].y) + (acc[0][1].x + acc[0][1].y);
                 float u1 = (acc[1][0].x + acc[1][0].y) + (acc[1][1].x + acc[1][1].y);
-                u0 += __shfl_xor_sync(0xffffffffu, u0, 1);
-                u1 += __shfl_xor_sync(0xffffffffu, u1, 1);
-                u0 += __shfl_xor_sync(0xffffffffu, u0, 2);
-                u1 += __shfl_xor_sync(0xffffffffu, u1, 2);
+#pragma unroll
+                for (int o = 1; o < kFoldTPR; o <<= 1) {   // the pair's TPR threads
+                    u0 += __shfl_xor_sync(0xffffffffu, u0, o);
+                    u1 += __shfl_xor_sync(0xffffffffu, u1, o);
+                }
                 const float rs = rsS[t], be = betaS[t];
                 const float v0 = to_f32<IO>(Xv[(size_t)t * kFoldRows + pair]);
                 const float v1 = to_f32<IO>(Xv[(size_t)t * kFoldRows + pair + kFoldPairs]);
@@ -345,7 +360,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                 float *drow = ckpt + (sh_hv * V + row0 + pair + rr * kFoldPairs) * K;
 #pragma unroll
                 for (int m = 0; m < kNC; ++m) {
-                    float4 *dst = reinterpret_cast<float4 *>(drow + (part + 4 * m) * kPer);
+                    float4 *dst = reinterpret_cast<float4 *>(drow + (part + kFoldTPR * m) * kPer);
 #pragma unroll
                     for (int q = 0; q < kPer / 4; ++q) {
                         const int i = m * (kPer / 2) + 2 * q;
@@ -376,7 +391,8 @@ static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n
     if (e != cudaSuccess) return e;
     // enough CTAs for every item of a typical step to run at once; the ones
     // without an item leave after the flag scan
-    kern<<<4 * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B, data_wait_limit());
+    kern<<<FoldGeom<K>::CtasPerSm * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B,
+                                                                        data_wait_limit());
     return cudaGetLastError();
 }
 

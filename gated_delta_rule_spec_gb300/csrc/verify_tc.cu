@@ -32,12 +32,13 @@
 // path; everything else is O(n) per thread or O(n^2) per CTA on CUDA cores.
 //
 // Data movement: each head's checkpoint tile (128 x 128 fp32 = 64 KiB) is the
-// bulk of the bytes.  The L2 prefetch of the tiles and of the ring's v
-// history is issued as soon as the cursors are known; every other global
-// read of the unit (keys, queries, gates, window values) is issued in one
-// round at the end of the previous unit.  The TMA tile loads into shared
-// memory are issued after the key buffers are dead, so a tile reuses their
-// space and the CTA needs ~73 KiB of shared memory: three CTAs per SM.
+// bulk of the bytes; it is read once, by a TMA load into shared memory issued
+// after the key buffers are dead, so a tile reuses their space and the CTA
+// needs ~73 KiB of shared memory: three CTAs per SM, which between them hide
+// the loads' DRAM latency.  The ring's v history is prefetched into L2 at the
+// start of the unit; every other global read of the unit (keys, queries,
+// gates, window values) is issued in one round at the end of the previous
+// unit.
 //
 // Side channel (sglang PR #36821 ring-write placement): the window's raw k
 // (one writer per k-head), raw v (each V-block its rows) and the fp32 g and
@@ -128,10 +129,9 @@ __device__ __forceinline__ float bf16_word_to_float(uint32_t w) { return __uint_
 
 // One unit = (batch row, block of 128 state rows, NH v-heads hv0 .. hv0 +
 // NH - 1 of one q/k head).  Fetching a unit means reading its slot and cursors
-// (one thread) and prefetching its checkpoint tiles and v histories into L2.
-// Inside the unit loop the fetch of the next unit is split into stages spread
-// over the current unit, so that no stage waits on a load: the slot index,
-// then the cursors, then the checks, the prefetch and the hand-over through
+// (one thread).  Inside the unit loop the fetch of the next unit is split into
+// stages spread over the current unit, so that no stage waits on a load: the
+// slot index, then the cursors, then the checks and the hand-over through
 // shared memory.
 struct UnitInfo {
     int slot, base, W, ok;
@@ -144,8 +144,28 @@ __device__ __forceinline__ void unit_coords(int u, int NP, int VB, int &bb, int 
     bb = rest / VB;
 }
 
-// Last stage: checks (status bits as row_cursor_ok sets them), L2 prefetch,
-// hand-over to dst[0..3].  wp and cbase are only read when the slot is in range.
+// L2 prefetch of a unit's v histories (one or two contiguous ring segments
+// per head when whole records are contiguous, V = 128).  The checkpoint tiles
+// are not prefetched: measured on the Qwen3-Next-shaped layer at B = 128, a
+// tile prefetched one unit (or half a unit) ahead of its TMA load was often
+// evicted from L2 before the load and read from DRAM twice (DRAM bytes 1.56x /
+// 1.10x of the algorithmic bytes against 1.00x without it, and the launch 20%
+// / 6% slower); the three resident CTAs hide the load's DRAM latency.
+template <int NH>
+__device__ __forceinline__ void prefetch_vhist(const LayerArgs &P, int slot, int cbase, int wp, int pr) {
+    if (P.V != kBV) return;
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+        const size_t sh_hv = (size_t)slot * P.HV + pr * NH + hh;
+        const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv) + sh_hv * P.L * P.V;
+        const int first = (P.L - cbase) < wp ? (P.L - cbase) : wp;
+        if (first > 0) ptx::prefetch_l2(rv + (size_t)cbase * P.V, first * P.V * 2);
+        if (wp > first) ptx::prefetch_l2(rv, (wp - first) * P.V * 2);
+    }
+}
+
+// Last stage: checks (status bits as row_cursor_ok sets them), hand-over to
+// dst[0..3].  wp and cbase are only read when the slot is in range.
 template <int NH>
 __device__ __forceinline__ void finish_fetch(const LayerArgs &P, const CursorArgs &C, int u,
                                              int nunits, int VB, int slot, int wp, int cbase,
@@ -165,19 +185,6 @@ __device__ __forceinline__ void finish_fetch(const LayerArgs &P, const CursorArg
         else ok = true;
     }
     if (st && vb == 0 && pr == 0) atomicOr(C.status, st);
-    if (ok) {  // checkpoint tiles and v histories into L2; used at the end of the unit
-#pragma unroll
-        for (int hh = 0; hh < NH; ++hh) {
-            const size_t sh_hv = (size_t)slot * P.HV + pr * NH + hh;
-            ptx::prefetch_l2(P.checkpoint + (sh_hv * P.V + vb * kBV) * kK, kBV * kK * 4);
-            const __nv_bfloat16 *rv = reinterpret_cast<const __nv_bfloat16 *>(P.rawv) + sh_hv * P.L * P.V;
-            if (P.V == kBV) {  // whole records are contiguous: one or two segments
-                const int first = (P.L - cbase) < wp ? (P.L - cbase) : wp;
-                if (first > 0) ptx::prefetch_l2(rv + (size_t)cbase * P.V, first * P.V * 2);
-                if (wp > first) ptx::prefetch_l2(rv, (wp - first) * P.V * 2);
-            }
-        }
-    }
     dst[0] = slot; dst[1] = ok ? cbase : 0; dst[2] = ok ? wp : 0; dst[3] = ok ? 1 : 0;
 }
 
@@ -373,6 +380,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
             unit_coords(un, NP, VB, bbn, prn, vbn);
             f_slot = slot_idx[bbn];
         }
+        if (ok && tid == 64) prefetch_vhist<NH>(P, slot, base, W, pr);   // used in phase 5
         float vt[NH][TM];
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh)
@@ -803,7 +811,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                 }
             }
             ptx::fence_proxy_async_smem();
-            if (tid == 32)   // fetch stage 3: checks, L2 prefetch, hand-over
+            if (tid == 32)   // fetch stage 3: checks, hand-over
                 finish_fetch<NH>(P, C, un, nunits, VB, f_slot, f_wp, f_base, misc);
         } else {
             if (tid == 0) fetch_unit<NH>(P, C, slot_idx, un, nunits, VB, misc);
