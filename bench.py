@@ -59,6 +59,16 @@ def verify_bytes_per_unit(W: np.ndarray, K: int, V: int, T: int, G: int, e: int,
     return V * K * 4 + W * rec + T * win_in + T * V * e + T * rec
 
 
+def verify_d_bytes_per_unit(W: np.ndarray, K: int, V: int, T: int, G: int, e: int) -> np.ndarray:
+    """Algorithmic HBM bytes of one derived-d verify per (row, v-head) unit:
+    checkpoint read, history records (fp32 d, raw k share, g, beta), window
+    inputs, outputs, the window's raw records and its fp32 d written."""
+    hist = V * 4 + K * e / G + 8
+    win_in = 2 * K * e / G + V * e + 2 * e
+    rec = V * e + K * e / G + 8
+    return V * K * 4 + W * hist + T * win_in + T * V * e + T * (rec + V * 4)
+
+
 def mirror_cursors(wp, base, acc_rows, T, L):
     """Host copy of the cursor arithmetic (commit then fold), used only to know
     each verify's ring fill W for byte accounting.  Returns W per step [steps, B]."""
@@ -207,13 +217,14 @@ class Workload:
         return d
 
 
-def build_state(wl: Workload, seed: int, device, random_rounds: int = 48):
+def build_state(wl: Workload, seed: int, device, random_rounds: int = 48, dring=None):
     """Layer state built by the library's own rounds from a zero checkpoint:
     16 full-accept rounds, then random_rounds with accept_len ~ U{1..T}.  During
     the random rounds each row first sits out a random number of rounds (accept
     0), drawn from [0, one fold cycle] (a cycle is about (L - 2T) / E[accept_len]
     rounds), so that the rows' ring fill levels and fold times spread out as in
-    a serving batch instead of moving in lockstep."""
+    a serving batch instead of moving in lockstep.  With a d ring the rounds
+    verify through gdn_spec_verify_d, which fills it."""
     import torch
     from gated_delta_rule_spec_gb300 import binding
     from gated_delta_rule_spec_gb300 import inputs as gen
@@ -238,7 +249,11 @@ def build_state(wl: Workload, seed: int, device, random_rounds: int = 48):
     pause = rng.integers(0, max(1, cycle), size=wl.B)
     for r in range(16 + random_rounds):
         w = dev_window()
-        binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias)
+        if dring is None:
+            binding.verify(layer, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias)
+        else:
+            binding.verify_d(layer, dring, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log,
+                             dt_bias)
         if r < 16:
             acc = full
         else:
@@ -716,6 +731,126 @@ def run_snapshot(args, rank: int, world: int) -> dict | None:
         "clocks": clocks,
     }
 
+# ----------------------------------------------------------------- derived-d comparison
+
+def run_derived_d(args, rank: int, world: int) -> dict | None:
+    """The derived-d ring (comparison variant: the ring also caches each token's
+    corrected delta, so verify solves only the window's system; with --window 1
+    the no-inverse decode): a step is gdn_spec_verify_d -> commit -> fold,
+    captured in CUDA graphs; the verify kernel is timed on its own as the
+    median of 10 replays of a graph of 20 calls."""
+    import torch
+    from gated_delta_rule_spec_gb300 import binding
+    from gated_delta_rule_spec_gb300 import inputs as gen
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    wl = Workload(args.batch, args.window)
+    name = wl.name.replace("-gdn-", "-gdn-derived-d-")
+    layer0 = binding.SpecLayer(wl.H, wl.HV, wl.K, wl.V, wl.T, wl.L, wl.num_slots, device=device)
+    dring = layer0.new_dring()
+    del layer0
+    rng, layer, cur, A_log, dt_bias, slots, dev_window = build_state(wl, 2000 + rank, device,
+                                                                     args.setup_rounds, dring=dring)
+    NI = 16
+    R = max(1, min(args.steps, 200))
+    inputs = [dev_window() for _ in range(NI)]
+    outs = [torch.empty(wl.B, wl.T, wl.HV, wl.V, dtype=torch.bfloat16, device=device) for _ in range(NI)]
+    acc_dev = torch.from_numpy(np.stack([gen.accept_lens(rng, wl.B, wl.T) for _ in range(R)])).to(device)
+
+    def vd(i):
+        w = inputs[i % NI]
+        binding.verify_d(layer, dring, cur, slots, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt_bias,
+                         out=outs[i % NI])
+
+    def step(i):
+        vd(i)
+        binding.commit(cur, wl.T, wl.L, slots, acc_dev[i % R])
+        binding.fold(layer, cur, slots)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graphs = {}
+    with torch.cuda.stream(side):
+        for gname, n in (("warm", args.warmup), ("chunk", R), ("rem", args.steps % R)):
+            if n == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    step(i)
+            graphs[gname] = g
+        gv = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gv, stream=side):
+            for i in range(20):
+                vd(i)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    if "warm" in graphs:
+        graphs["warm"].replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    e0.record()
+    for _ in range(args.steps // R):
+        graphs["chunk"].replay()
+    if "rem" in graphs:
+        graphs["rem"].replay()
+    e1.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    W_now = cur.write_pos[slots.long()].cpu().numpy().astype(np.int64)
+    times = []
+    for _ in range(10):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record()
+        gv.replay()
+        b_.record()
+        torch.cuda.synchronize()
+        times.append(a_.elapsed_time(b_) / 20)
+    v_ms = statistics.median(times)
+    status = binding.read_status(cur)
+    if world > 1:
+        ms, = reduce_max([ms], device)
+    if rank != 0:
+        return None
+    byts = float(verify_d_bytes_per_unit(W_now, wl.K, wl.V, wl.T, wl.G, wl.e).sum() * wl.HV)
+    peaks, peak_kind = measured_peaks()
+    achieved = byts / (v_ms / 1e3) / 1e9
+    return {
+        "metric": METRIC, "variant": "derived-d (comparison: the ring also caches each token's corrected delta)",
+        "value": round(world * wl.B * wl.T * args.steps / (ms / 1e3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
+        "config": wl.config({"workload": name, "arith": ARITH["tc"],
+                             "step": "verify_d + commit + fold", "mean_ring_fill_W": round(float(W_now.mean()), 2),
+                             "d_ring_bytes": int(dring.numel() * 4)}),
+        "gpu_launches": 4 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": round(byts), "kernel": "verify_d",
+                     "peak_kind": peak_kind, "verify_us": round(v_ms * 1e3, 2),
+                     "verify_timing": "median of 10 replays of a CUDA graph of 20 verify_d calls",
+                     "verify_us_replays": [round(x * 1e3, 2) for x in times]},
+        "verify_tokens_per_s": round(wl.B * wl.T / (v_ms / 1e3), 1),
+        "device_status": status,
+        "clocks": clocks,
+    }
+
+
 # ----------------------------------------------------------------- prefill
 
 PREFILL_METRIC = "prefilled tokens/s per GDN layer, 1\u00d7GB300"
@@ -912,8 +1047,12 @@ def run_reference(args, rank: int, world: int) -> dict | None:
                                                 w["b"], A_log, dt)
             oracle.snapshot_commit(d, ly, slot_idx, accs[i % 4], snap)
             return
-        oracle.verify(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
-                      nthreads=cores)
+        if args.variant == "derived-d":   # the same outputs, plus the window's d
+            oracle.verify_d(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
+                            nthreads=cores)
+        else:
+            oracle.verify(d, ly, cur, slot_idx, w["q"], w["k"], w["v"], w["a"], w["b"], A_log, dt,
+                          nthreads=cores)
         oracle.commit(d, cur, slot_idx, accs[i % 4])
         oracle.fold(d, ly, cur, slot_idx, nthreads=cores)
 
@@ -930,6 +1069,9 @@ def run_reference(args, rank: int, world: int) -> dict | None:
     extra = {"sample_rows_per_step": rows}
     if snapshot:
         extra.update(workload=wl.name.replace("-verify-", "-snapshot-verify-"), step=what)
+    if args.variant == "derived-d":
+        extra.update(workload=wl.name.replace("-gdn-", "-gdn-derived-d-"),
+                     step="verify_d + commit + fold")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
@@ -955,8 +1097,9 @@ def main():
                     help="draft window T (default: the workload's 4; 1 = plain decode)")
     ap.add_argument("--kda", action="store_true",
                     help="the KDA variant (one gate per key channel) on the same shape")
-    ap.add_argument("--variant", choices=("ring", "snapshot"), default="ring",
-                    help="snapshot: the per-draft state design the ring replaces (comparison)")
+    ap.add_argument("--variant", choices=("ring", "snapshot", "derived-d"), default="ring",
+                    help="snapshot: the per-draft state design the ring replaces; derived-d: the "
+                         "ring also caches each token's corrected delta (comparisons)")
     ap.add_argument("--prefill", type=int, default=0, metavar="N",
                     help="measure gdn_spec_prefill of --batch prompts of N tokens instead")
     ap.add_argument("--verify-only", action="store_true",
@@ -993,6 +1136,8 @@ def main():
                             "d2h_bytes_per_step": 0}}
     elif args.variant == "snapshot" and args.impl != "reference":
         line = run_snapshot(args, rank, world)
+    elif args.variant == "derived-d" and args.impl != "reference":
+        line = run_derived_d(args, rank, world)
     elif args.prefill:
         line = run_prefill(args, rank, world)
         if line is not None and world == 1 and not args.no_cpu_baseline:

@@ -49,7 +49,8 @@ class CursorDesc(ctypes.Structure):
 
 
 _lib = None
-EXPORTS = ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset", "gdn_spec_prefill",
+EXPORTS = ("gdn_spec_verify", "gdn_spec_verify_d", "gdn_spec_commit", "gdn_spec_fold",
+           "gdn_spec_reset", "gdn_spec_prefill",
            "gdn_spec_snapshot_verify", "gdn_spec_snapshot_commit",
            "gdn_spec_read_status", "gdn_spec_strerror", "gdn_spec_abi_version",
            "gdn_spec_verify_path", "gdn_spec_set_wait_limit")
@@ -73,6 +74,7 @@ def load() -> ctypes.CDLL:
     P, I32 = ctypes.c_void_p, ctypes.c_int32
     LP, CP = ctypes.POINTER(LayerDesc), ctypes.POINTER(CursorDesc)
     lib.gdn_spec_verify.argtypes = [LP, CP, P, I32, P, P, P, P, P, P, P, P, P]
+    lib.gdn_spec_verify_d.argtypes = [LP, P, CP, P, I32, P, P, P, P, P, P, P, P, P]
     lib.gdn_spec_commit.argtypes = [CP, I32, I32, P, I32, P, P]
     lib.gdn_spec_fold.argtypes = [LP, I32, CP, P, I32, P]
     lib.gdn_spec_reset.argtypes = [CP, P, I32, P]
@@ -80,7 +82,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_spec_snapshot_verify.argtypes = [LP, CP, P, I32, P, P, P, P, P, P, P, P, P, P]
     lib.gdn_spec_snapshot_commit.argtypes = [LP, CP, P, I32, P, P, P]
     lib.gdn_spec_read_status.argtypes = [CP, ctypes.POINTER(ctypes.c_uint32), I32, P]
-    for name in ("gdn_spec_verify", "gdn_spec_commit", "gdn_spec_fold", "gdn_spec_reset",
+    for name in ("gdn_spec_verify", "gdn_spec_verify_d", "gdn_spec_commit", "gdn_spec_fold",
+                 "gdn_spec_reset",
                  "gdn_spec_prefill", "gdn_spec_snapshot_verify", "gdn_spec_snapshot_commit",
                  "gdn_spec_read_status"):
         getattr(lib, name).restype = ctypes.c_int
@@ -159,6 +162,11 @@ class SpecLayer:
                          self.rawv.data_ptr(), self.rawk.data_ptr(), self.ring_g.data_ptr(),
                          self.ring_beta.data_ptr())
 
+    def new_dring(self) -> torch.Tensor:
+        """A zeroed d ring for gdn_spec_verify_d: fp32 [num_slots, HV, L, V]."""
+        return torch.zeros(self.num_slots, self.HV, self.L, self.V, dtype=torch.float32,
+                           device=self.checkpoint.device)
+
     def window_shapes(self, B: int) -> dict:
         T, H, HV, K, V = self.T, self.H, self.HV, self.K, self.V
         return {"q": (B, T, H, K), "k": (B, T, H, K), "v": (B, T, HV, V),
@@ -192,6 +200,32 @@ def verify(layer: SpecLayer, cursors: SpecCursors, slot_idx: torch.Tensor, q, k,
                                 _ptr(slot_idx), B, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
                                 _ptr(A_log), _ptr(dt_bias), _ptr(out), _stream(stream))
     _check(rc, "gdn_spec_verify")
+    return out
+
+
+def verify_d(layer: SpecLayer, dring: torch.Tensor, cursors: SpecCursors, slot_idx: torch.Tensor,
+             q, k, v, a, b, A_log, dt_bias, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """gdn_spec_verify_d (comparison variant): outputs of the draft window
+    [B, T, HV, V] from a ring that also caches each token's corrected delta;
+    writes the window's raw records into the ring and its d into ``dring``
+    (fp32 [num_slots, HV, L, V], see ``SpecLayer.new_dring``)."""
+    B = slot_idx.shape[0]
+    shp = layer.window_shapes(B)
+    io = layer.io_torch
+    _need(slot_idx, "slot_idx", torch.int32, (B,))
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b)):
+        _need(t, name, io, shp[name])
+    _need(A_log, "A_log", torch.float32, shp["A_log"])
+    _need(dt_bias, "dt_bias", torch.float32, shp["dt_bias"])
+    _need(dring, "dring", torch.float32, (layer.num_slots, layer.HV, layer.L, layer.V))
+    if out is None:
+        out = torch.empty(shp["out"], dtype=io, device=q.device)
+    _need(out, "out", io, shp["out"])
+    rc = load().gdn_spec_verify_d(ctypes.byref(layer.desc()), _ptr(dring), ctypes.byref(cursors.desc()),
+                                  _ptr(slot_idx), B, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
+                                  _ptr(A_log), _ptr(dt_bias), _ptr(out), _stream(stream))
+    _check(rc, "gdn_spec_verify_d")
     return out
 
 

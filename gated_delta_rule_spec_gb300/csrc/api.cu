@@ -41,6 +41,11 @@ cudaError_t launch_prefill(const LayerArgs &P, const CursorArgs &C, bool kda, bo
                            const void *v, const void *a, const void *b, const float *A_log,
                            const float *dt_bias, void *out, int from_zero, cudaStream_t stream);
 size_t prefill_smem_bytes(int K, bool kda, bool bf16);
+bool verify_d_supported(const LayerArgs &P, bool kda, bool bf16);
+cudaError_t launch_verify_d(const LayerArgs &P, const CursorArgs &C, float *dring,
+                            const int32_t *slot_idx, int B, const void *q, const void *k,
+                            const void *v, const void *a, const void *b, const float *A_log,
+                            const float *dt_bias, void *out, cudaStream_t stream);
 cudaError_t launch_snapshot_verify(const LayerArgs &P, const CursorArgs &C, bool kda, bool bf16,
                                    const int32_t *slot_idx, int B, const void *q, const void *k,
                                    const void *v, const void *a, const void *b, const float *A_log,
@@ -165,6 +170,28 @@ int gdn_spec_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors
     if (verify_generic_smem_bytes(P.K, P.L, P.T, kda) > kMaxSmem) return GDN_SPEC_EUNSUPPORTED;
     return cuda_rc(launch_verify_generic(P, C, kda, bf16, slot_idx, B, q, k, v, a, b, A_log,
                                          dt_bias, out, st));
+}
+
+int gdn_spec_verify_d(const gdn_spec_layer *layer, float *dring, const gdn_spec_cursors *cursors,
+                      const int32_t *slot_idx, int32_t B, const void *q, const void *k,
+                      const void *v, const void *a, const void *b, const float *A_log,
+                      const float *dt_bias, void *out, void *stream) {
+    int rc = check_layer(layer);
+    if (rc) return rc;
+    if ((rc = check_cursors(cursors))) return rc;
+    if (cursors->num_slots != layer->num_slots) return GDN_SPEC_EINVAL;
+    if (B < 0) return GDN_SPEC_EINVAL;
+    if (B == 0) return GDN_SPEC_OK;
+    if (!dring || !slot_idx || !q || !k || !v || !a || !b || !A_log || !dt_bias || !out)
+        return GDN_SPEC_EINVAL;
+    if (!aligned16(dring) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return GDN_SPEC_EALIGN;
+    const LayerArgs P = layer_args(layer);
+    const bool kda = layer->gate_kind == GDN_SPEC_GATE_PER_KEY;
+    const bool bf16 = layer->io_dtype == GDN_SPEC_DTYPE_BF16;
+    if (!verify_d_supported(P, kda, bf16)) return GDN_SPEC_EUNSUPPORTED;
+    return cuda_rc(launch_verify_d(P, cursor_args(cursors), dring, slot_idx, B, q, k, v, a, b, A_log,
+                                   dt_bias, out, static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_spec_commit(const gdn_spec_cursors *cursors, int32_t T, int32_t L,

@@ -67,8 +67,9 @@ extern "C" {
 #endif
 
 #define GDN_SPEC_ABI_VERSION 3   /* 2: adds gdn_spec_prefill and the snapshot comparison calls;
-                                    3: adds gdn_spec_set_wait_limit, commit's cursor check and the
-                                       poisoning of rows a fold or prefill could not finish */
+                                    3: adds gdn_spec_verify_d, gdn_spec_set_wait_limit, commit's
+                                       cursor check and the poisoning of rows a fold or prefill
+                                       could not finish */
 
 /* host-side error codes (return values) */
 #define GDN_SPEC_OK            0
@@ -159,6 +160,29 @@ int gdn_spec_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors
                     const void *q, const void *k, const void *v, const void *a,
                     const void *b, const float *A_log, const float *dt_bias, void *out,
                     void *stream);
+
+/*
+ * gdn_spec_verify_d -- comparison variant of gdn_spec_verify for a ring that
+ * also caches every token's corrected delta d_t = beta_t (v_t - S_t^- k^_t)
+ * (S_t^- the state after token t's decay): the first design of [blog] §12.1
+ * and appendix A.1.  With the history's d cached the verify solves only the
+ * window's T x T system; with T = 1 (plain decode) no system at all ([blog]
+ * §12.2, §12.9, Part A).  Outputs as gdn_spec_verify; writes the window's raw
+ * records into the ring and the window's d into `dring` at the same positions
+ * (cache_base + write_pos + s) & (L-1).  The checkpoint and cursors are only
+ * read; commit, fold (which replays the raw records, so the cached d never
+ * reach the checkpoint) and reset are the ring path's.  A layer that uses it
+ * must use it for every verify since its last prefill or reset, so that
+ * every committed record's d is in the d ring.
+ *   dring  fp32 [num_slots, HV, L, V]   (caller-owned device memory)
+ *   other arguments as gdn_spec_verify.
+ * Supported shapes: bf16 I/O, GATE_SCALAR, K = 128, V a multiple of 128,
+ * L <= 64, T <= 8; otherwise GDN_SPEC_EUNSUPPORTED.
+ */
+int gdn_spec_verify_d(const gdn_spec_layer *layer, float *dring, const gdn_spec_cursors *cursors,
+                      const int32_t *slot_idx, int32_t B, const void *q, const void *k,
+                      const void *v, const void *a, const void *b, const float *A_log,
+                      const float *dt_bias, void *out, void *stream);
 
 /*
  * gdn_spec_commit -- after sampling: for each row with a slot,

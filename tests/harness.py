@@ -182,6 +182,28 @@ class Scenario:
                                       unit_mask=unit_mask, nthreads=NTHREADS)
         return out, o_orc, st
 
+    def verify_d(self, w, dring: torch.Tensor):
+        """gdn_spec_verify_d against the oracle's verify_d: returns (out device,
+        out oracle, d of the window from the device's d ring [B, T, HV, V],
+        d of the window from the oracle, status)."""
+        d = self.dims
+        wp, base = to_host(self.cur.write_pos), to_host(self.cur.cache_base)
+        dev = {name: to_dev(x) for name, x in w.items()}
+        out = binding.verify_d(self.layer, dring, self.cur, self.slot_dev, dev["q"], dev["k"], dev["v"],
+                               dev["a"], dev["b"], self.A_log_dev, self.dt_bias_dev)
+        f = {name: gen.to_f64(x) for name, x in w.items()}
+        o_orc, d_orc, st = oracle.verify_d(self.dims, self.orc, self.orc_cur, self.slot_idx, f["q"],
+                                           f["k"], f["v"], f["a"], f["b"], self.A_log, self.dt_bias,
+                                           nthreads=NTHREADS)
+        host = to_host(dring)
+        d_dev = np.zeros((self.B, d.T, d.HV, d.V), np.float64)
+        for i, slot in enumerate(self.slot_idx):
+            if 0 <= slot < self.num_slots:
+                for s in range(d.T):
+                    p = (int(base[slot]) + int(wp[slot]) + s) & (d.L - 1)
+                    d_dev[i, s] = host[slot, :, p]
+        return out, o_orc, d_dev, d_orc, st
+
     def commit(self, acc: np.ndarray):
         binding.commit(self.cur, self.dims.T, self.dims.L, self.slot_dev, to_dev(acc))
         return oracle.commit(self.dims, self.orc_cur, self.slot_idx, acc)

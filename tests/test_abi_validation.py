@@ -158,3 +158,23 @@ def test_prefill_and_snapshot_errors(lib):
     assert snap_c(0) == OK
     assert snap_c(1, acc=None) == EINVAL
     assert snap_c(1, snap=MIS) == EALIGN
+
+
+def verify_d(lib, ly, cu, B=1, dring=FAKE, slot=FAKE, q=FAKE, out=FAKE):
+    return lib.gdn_spec_verify_d(_ref(ly), dring, _ref(cu), slot, B, q, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                 FAKE, out, None)
+
+
+def test_verify_d_errors(lib):
+    """The derived-d comparison variant: the tensor-core shapes only, a d ring
+    that is present and 16-byte aligned, and the verify call's other checks."""
+    ly, cu = layer(), cursors()
+    assert verify_d(lib, ly, cu, B=0) == OK
+    assert verify_d(lib, ly, cu, dring=None) == EINVAL
+    assert verify_d(lib, ly, cu, dring=MIS) == EALIGN
+    assert verify_d(lib, ly, None) == EINVAL
+    assert verify_d(lib, ly, cu, q=MIS) == EALIGN
+    assert verify_d(lib, layer(HV=24), cu) == EINVAL
+    for kw in (dict(io_dtype=binding.DTYPE_FP32), dict(gate_kind=binding.GATE_PER_KEY),
+               dict(K=64), dict(L=128), dict(T=9, L=64), dict(V=96)):
+        assert verify_d(lib, layer(**kw), cu) == EUNSUP, kw
