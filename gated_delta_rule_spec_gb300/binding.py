@@ -53,7 +53,7 @@ EXPORTS = ("gdn_spec_verify", "gdn_spec_verify_d", "gdn_spec_commit", "gdn_spec_
            "gdn_spec_reset", "gdn_spec_prefill",
            "gdn_spec_snapshot_verify", "gdn_spec_snapshot_commit",
            "gdn_spec_read_status", "gdn_spec_strerror", "gdn_spec_abi_version",
-           "gdn_spec_verify_path", "gdn_spec_set_wait_limit")
+           "gdn_spec_verify_path", "gdn_spec_prefill_path", "gdn_spec_set_wait_limit")
 
 
 def library_path() -> str:
@@ -93,6 +93,8 @@ def load() -> ctypes.CDLL:
     lib.gdn_spec_abi_version.restype = ctypes.c_int
     lib.gdn_spec_verify_path.argtypes = [LP]
     lib.gdn_spec_verify_path.restype = ctypes.c_char_p
+    lib.gdn_spec_prefill_path.argtypes = [LP]
+    lib.gdn_spec_prefill_path.restype = ctypes.c_char_p
     lib.gdn_spec_set_wait_limit.argtypes = [ctypes.c_uint32]
     lib.gdn_spec_set_wait_limit.restype = ctypes.c_uint32
     _lib = lib
@@ -177,6 +179,13 @@ class SpecLayer:
 
 def verify_path(layer: SpecLayer) -> str:
     r = load().gdn_spec_verify_path(ctypes.byref(layer.desc()))
+    if r is None:
+        raise GdnSpecError("invalid layer descriptor")
+    return r.decode()
+
+
+def prefill_path(layer: SpecLayer) -> str:
+    r = load().gdn_spec_prefill_path(ctypes.byref(layer.desc()))
     if r is None:
         raise GdnSpecError("invalid layer descriptor")
     return r.decode()

@@ -41,6 +41,7 @@ cudaError_t launch_prefill(const LayerArgs &P, const CursorArgs &C, bool kda, bo
                            const void *v, const void *a, const void *b, const float *A_log,
                            const float *dt_bias, void *out, int from_zero, cudaStream_t stream);
 size_t prefill_smem_bytes(int K, bool kda, bool bf16);
+bool prefill_tc_supported(const LayerArgs &P, bool kda, bool bf16);
 bool verify_d_supported(const LayerArgs &P, bool kda, bool bf16);
 cudaError_t launch_verify_d(const LayerArgs &P, const CursorArgs &C, float *dring,
                             const int32_t *slot_idx, int B, const void *q, const void *k,
@@ -146,6 +147,14 @@ const char *gdn_spec_verify_path(const gdn_spec_layer *layer) {
     const bool kda = layer->gate_kind == GDN_SPEC_GATE_PER_KEY;
     const bool bf16 = layer->io_dtype == GDN_SPEC_DTYPE_BF16;
     return verify_tc_supported(P, kda, bf16) ? "tc" : "generic";
+}
+
+const char *gdn_spec_prefill_path(const gdn_spec_layer *layer) {
+    if (check_layer(layer) != GDN_SPEC_OK) return nullptr;
+    const LayerArgs P = layer_args(layer);
+    const bool kda = layer->gate_kind == GDN_SPEC_GATE_PER_KEY;
+    const bool bf16 = layer->io_dtype == GDN_SPEC_DTYPE_BF16;
+    return prefill_tc_supported(P, kda, bf16) ? "chunk" : "sequential";
 }
 
 int gdn_spec_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors,

@@ -32,6 +32,12 @@
 
 namespace gdnspec {
 
+bool prefill_tc_supported(const LayerArgs &P, bool kda, bool bf16);
+cudaError_t launch_prefill_tc(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx, int B,
+                              int N, const void *q, const void *k, const void *v, const void *a,
+                              const void *b, const float *A_log, const float *dt_bias, void *out,
+                              int from_zero, cudaStream_t stream);
+
 constexpr int kPreThreads = 128;
 constexpr int kPreTPR = 4;                          // threads per pair of state rows
 constexpr int kPrePairs = kPreThreads / kPreTPR;    // 32
@@ -102,6 +108,7 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
     const long long nitems = (long long)B * HV * vblocks;
     const int pair = tid / kPreTPR, part = tid % kPreTPR;
     uint32_t phase = 0;
+    bool failed = false;   // a wait ran out: the rows of the remaining items are only marked
 
     if (tid == 0) {
         ptx::mbar_init(bar, 1);
@@ -129,6 +136,10 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
             }
             continue;
         }
+        if (failed) {   // an earlier item's wait ran out: not computed, poisoned by the cursor kernel
+            if (!SNAP && tid == 0) C.is_flush[slot] = kFoldFailed;
+            continue;
+        }
         const size_t sh_hv = (size_t)slot * HV + hv;
         float *ckpt = P.checkpoint;
         const bool valid0 = pair < nrows, valid1 = pair + kPrePairs < nrows;
@@ -154,7 +165,6 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
             }
         }
         float gam = 1.0f, inv = 1.0f;   // scalar gate: S = gam R (every thread holds the same values)
-        bool failed = false;
 
         for (int c0 = 0; c0 < N; c0 += kPreChunk) {
             const int nt = N - c0 < kPreChunk ? N - c0 : kPreChunk;
@@ -359,7 +369,7 @@ prefill_kernel(LayerArgs P, CursorArgs C, const int32_t *__restrict__ slot_idx, 
             }
             __syncthreads();   // the chunk's buffers are reused by the next chunk
         }
-        if (failed) return;
+        if (failed) continue;
         if (SNAP) continue;   // the snapshot variant only reads the checkpoint
 
         // ---- 5. S = gam R into the checkpoint
@@ -427,6 +437,13 @@ __global__ void snapshot_commit_kernel(LayerArgs P, CursorArgs C, const int32_t 
     for (size_t i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
 }
 
+static cudaError_t launch_prefill_cursors(const CursorArgs &C, int L, const int32_t *slot_idx, int B,
+                                          int from_zero, cudaStream_t stream) {
+    const int cb = (B + 255) / 256;
+    prefill_cursor_kernel<<<cb < 1 ? 1 : (cb > 64 ? 64 : cb), 256, 0, stream>>>(C, L, slot_idx, B, from_zero);
+    return cudaGetLastError();
+}
+
 template <typename IO, bool KDA, int K, bool SNAP>
 static cudaError_t launch_prefill_k(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
                                     int B, int N, const void *q, const void *k, const void *v,
@@ -451,10 +468,7 @@ static cudaError_t launch_prefill_k(const LayerArgs &P, const CursorArgs &C, con
             dt_bias, static_cast<IO *>(out), from_zero, snap, data_wait_limit());
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (SNAP) return cudaSuccess;
-    const int cb = (B + 255) / 256;
-    prefill_cursor_kernel<<<cb < 1 ? 1 : (cb > 64 ? 64 : cb), 256, 0, stream>>>(C, P.L, slot_idx, B,
-                                                                                 from_zero);
-    return cudaGetLastError();
+    return launch_prefill_cursors(C, P.L, slot_idx, B, from_zero, stream);
 }
 
 template <typename IO, bool KDA, bool SNAP>
@@ -488,6 +502,12 @@ cudaError_t launch_prefill(const LayerArgs &P, const CursorArgs &C, bool kda, bo
                            const int32_t *slot_idx, int B, int N, const void *q, const void *k,
                            const void *v, const void *a, const void *b, const float *A_log,
                            const float *dt_bias, void *out, int from_zero, cudaStream_t stream) {
+    if (prefill_tc_supported(P, kda, bf16)) {   // chunk-parallel form on the tensor cores
+        cudaError_t e = launch_prefill_tc(P, C, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out,
+                                          from_zero, stream);
+        if (e != cudaSuccess) return e;
+        return launch_prefill_cursors(C, P.L, slot_idx, B, from_zero, stream);
+    }
     return launch_any<false>(P, C, kda, bf16, slot_idx, B, N, q, k, v, a, b, A_log, dt_bias, out,
                              from_zero, nullptr, stream);
 }

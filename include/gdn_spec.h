@@ -66,10 +66,11 @@
 extern "C" {
 #endif
 
-#define GDN_SPEC_ABI_VERSION 3   /* 2: adds gdn_spec_prefill and the snapshot comparison calls;
+#define GDN_SPEC_ABI_VERSION 4   /* 2: adds gdn_spec_prefill and the snapshot comparison calls;
                                     3: adds gdn_spec_verify_d, gdn_spec_set_wait_limit, commit's
                                        cursor check and the poisoning of rows a fold or prefill
-                                       could not finish */
+                                       could not finish;
+                                    4: adds gdn_spec_prefill_path and the chunk-parallel prefill */
 
 /* host-side error codes (return values) */
 #define GDN_SPEC_OK            0
@@ -225,11 +226,17 @@ int gdn_spec_reset(const gdn_spec_cursors *cursors, const int32_t *slot_idx, int
  * gdn_spec_prefill -- prefill of each row's N prompt tokens into its slot
  * (the step before decode; the reset of the prefill -> decode handoff,
  * [blog] appendix A.2, is part of it): for every v-head the recurrence runs
- * over the tokens, token by token in fp32 as the fold does, from a zero
- * state (from_zero != 0) or from the slot's checkpoint (from_zero == 0, which
- * gives chunked prefill across calls); every token's output is written, the
- * final state becomes the slot's checkpoint, and the slot's cursors are reset
- * (write_pos = cache_base = is_flush = 0).  The ring is not written.
+ * over the tokens from a zero state (from_zero != 0) or from the slot's
+ * checkpoint (from_zero == 0, which gives chunked prefill across calls);
+ * every token's output is written, the final state becomes the slot's
+ * checkpoint, and the slot's cursors are reset (write_pos = cache_base =
+ * is_flush = 0).  The ring is not written.  Two kernels (gdn_spec_prefill_path
+ * names the one a layer uses): "chunk" -- scalar gate, bf16 I/O, K = 128 and V
+ * a multiple of 128 -- the chunk-parallel UT form on the tensor cores, 64
+ * tokens per step ([blog] appendix B.1 names chunk_gated_delta_rule as the
+ * prefill authority; tf32 operands, the state update split into tf32 high and
+ * low parts); "sequential" -- every other shape, token by token in fp32 as
+ * the fold does.
  *   q, k      io_dtype [B, N, H, K]
  *   v         io_dtype [B, N, HV, V]
  *   a         io_dtype [B, N, HV]   (GATE_PER_KEY: [B, N, HV, K])
@@ -307,6 +314,12 @@ int gdn_spec_abi_version(void);
  * ("tc" = TMA + tcgen05 path, "generic" = CUDA-core path), or NULL if the
  * layer is invalid.  Host only; launches nothing. */
 const char *gdn_spec_verify_path(const gdn_spec_layer *layer);
+
+/* Name of the prefill kernel gdn_spec_prefill would launch for this layer
+ * ("chunk" = chunk-parallel tensor-core path, "sequential" = token-by-token
+ * CUDA-core path), or NULL if the layer is invalid.  Host only; launches
+ * nothing. */
+const char *gdn_spec_prefill_path(const gdn_spec_layer *layer);
 
 #ifdef __cplusplus
 }

@@ -85,6 +85,21 @@ def test_verify_path_by_shape(lib, kw, path):
     assert lib.gdn_spec_verify_path(ctypes.byref(layer(**kw))) == path
 
 
+@pytest.mark.parametrize("kw,path", [
+    (dict(), b"chunk"),                                     # the Qwen3-Next shape
+    (dict(V=256), b"chunk"),
+    (dict(L=128), b"chunk"),                                # prefill does not use the ring
+    (dict(gate_kind=binding.GATE_PER_KEY), b"sequential"), # KDA
+    (dict(io_dtype=binding.DTYPE_FP32), b"sequential"),
+    (dict(K=64), b"sequential"),
+    (dict(V=96), b"sequential"),
+])
+def test_prefill_path_by_shape(lib, kw, path):
+    lib.gdn_spec_prefill_path.restype = ctypes.c_char_p
+    assert lib.gdn_spec_prefill_path(ctypes.byref(layer(**kw))) == path
+    assert lib.gdn_spec_prefill_path(ctypes.byref(layer(K=36))) is None
+
+
 def test_verify_call_errors(lib):
     ly, cu = layer(), cursors()
     assert verify(lib, ly, None) == EINVAL

@@ -85,6 +85,7 @@ def test_prefill_qwen3next_shape_then_continue(per_key):
     interleaving of slots."""
     c = PrefillCase(H=16, HV=32, K=128, V=128, L=64, num_slots=6, io=gen.BF16, per_key=per_key,
                     seed=61 + per_key)
+    assert binding.prefill_path(c.layer) == ("sequential" if per_key else "chunk")
     slots = np.array([5, 1, -1, 3], np.int32)
     out, o_orc, st, st_orc = c.prefill(slots, c.prompt(4, 150), from_zero=True)
     assert st == st_orc == 0
@@ -103,6 +104,7 @@ def test_prefill_qwen3next_shape_then_continue(per_key):
 
 def test_prefill_fp32_small_heads_error_is_a_number():
     c = PrefillCase(H=2, HV=4, K=32, V=40, L=16, num_slots=3, io=gen.FP32, per_key=False, seed=71)
+    assert binding.prefill_path(c.layer) == "sequential"
     slots = np.array([2, 0], np.int32)
     out, o_orc, st, _ = c.prefill(slots, c.prompt(2, 97), from_zero=True)
     assert st == 0
