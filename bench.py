@@ -98,7 +98,12 @@ ARITH = {
     "tc": "fp32; the Gram and the checkpoint product on tensor cores with tf32 operands "
           "and fp32 accumulation",
     "generic": "fp32 on CUDA cores",
+    "chunk": "fp32; the chunk's Gram (bf16 operands), the state products and the update (tf32 "
+             "operands, the update split into high and low parts) on tensor cores with fp32 "
+             "accumulation; the triangular solve on CUDA cores",
 }
+# tf32 dense tensor peak as a fraction of the bf16 one (nominal 1.1 / 2.25 PFLOP/s)
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
 def profiled_traffic(path_name: str, B: int, T: int, algorithmic_bytes: float):
@@ -862,6 +867,19 @@ def _prefill_flops(B: int, N: int, wl: "Workload") -> float:
     return 6.0 * wl.V * wl.K * B * N * wl.HV
 
 
+def _prefill_chunk_flops(B: int, N: int, wl: "Workload", C: int = 64) -> float:
+    """Algorithmic tensor flops of one chunk-parallel prefill call: per (row,
+    v-head) and chunk of n tokens the Gram [K; Q] K^T (2 K 2n n), the state
+    products S [K; Q]^T (2 V K 2n), the intra-chunk outputs D W^T (2 V n n)
+    and the state update D K (2 V K n).  The high/low split of the update is
+    not counted."""
+    total = 0.0
+    for c0 in range(0, N, C):
+        n = min(C, N - c0)
+        total += 2.0 * wl.K * 2 * n * n + 2.0 * wl.V * wl.K * 2 * n + 2.0 * wl.V * n * n + 2.0 * wl.V * wl.K * n
+    return total * B * wl.HV
+
+
 def run_prefill(args, rank: int, world: int) -> dict | None:
     """gdn_spec_prefill of B prompts of N tokens (from a zero state) on the
     Qwen3-Next-shaped layer, timed in CUDA graphs, plus an end-to-end leg
@@ -948,10 +966,23 @@ def run_prefill(args, rank: int, world: int) -> dict | None:
         return None
     t_call = ms / 1e3 / calls
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    peaks, _ = measured_peaks()
-    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12    # fp32 FMA lanes x 2 flops x clock, TFLOP/s
-    achieved = _prefill_flops(B, N, wl) / t_call / 1e12
+    peaks, peak_src = measured_peaks()
+    path = binding.prefill_path(layer)
+    if path == "chunk":
+        peak = float(peaks["bf16_tflops"]) * TF32_OVER_BF16
+        roofline = {"bound": "tensor", "achieved": round(_prefill_chunk_flops(B, N, wl) / t_call / 1e12, 2),
+                    "peak": round(peak, 2), "unit": "TFLOP/s", "traffic": None,
+                    "kernel": "prefill_tc_kernel (chunk-parallel)",
+                    "peak_kind": f"{peak_src} bf16 dense x nominal tf32/bf16 ratio (1.1/2.25)"}
+    else:
+        sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12    # fp32 FMA lanes x 2 flops x clock, TFLOP/s
+        roofline = {"bound": "alu", "achieved": round(_prefill_flops(B, N, wl) / t_call / 1e12, 2),
+                    "peak": round(peak, 2), "unit": "TFLOP/s", "traffic": None,
+                    "kernel": "prefill_kernel (sequential)",
+                    "peak_kind": "derived: SMs x 128 fp32 lanes x 2 x max SM clock"}
+    roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 4)
+    roofline["us_per_call"] = round(t_call * 1e6, 2)
     h2d = sum(t.numel() * t.element_size() for t in hin.values())
     return {
         "metric": PREFILL_METRIC, "value": round(world * B * N / t_call, 1), "unit": "tokens/s",
@@ -960,7 +991,7 @@ def run_prefill(args, rank: int, world: int) -> dict | None:
         "data": "synthetic (seeded; Qwen3-Next-shaped GDN layer, random weights)",
         "config": {"workload": f"qwen3next-gdn-prefill-b{B}-n{N}", "B": B, "N": N, "H": wl.H,
                    "HV": wl.HV, "K": wl.K, "V": wl.V, "io_dtype": "bf16", "state_dtype": "fp32",
-                   "arith": ARITH["generic"],
+                   "arith": ARITH["chunk" if path == "chunk" else "generic"], "path": path,
                    "step": "prefill from a zero state (outputs, checkpoint, cursor reset)",
                    "parallelism": "replicas"},
         "e2e": {"value": round(world * B * N * K_e2e / (e2e_ms / 1e3), 1), "unit": "tokens/s",
@@ -968,11 +999,7 @@ def run_prefill(args, rank: int, world: int) -> dict | None:
                 "d2h_bytes_per_step": int(hout.numel() * hout.element_size()), "steps": K_e2e,
                 "api": "python binding -> C ABI, host pinned buffers"},
         "gpu_launches": 2 * calls,
-        "roofline": {"bound": "alu", "achieved": round(achieved, 2),
-                     "peak": round(alu_peak, 2), "unit": "TFLOP/s",
-                     "frac": round(achieved / alu_peak, 4), "traffic": None,
-                     "kernel": "prefill", "peak_kind": "derived: SMs x 128 fp32 lanes x 2 x max SM clock",
-                     "us_per_call": round(t_call * 1e6, 2)},
+        "roofline": roofline,
         "clocks": clocks,
     }
 

@@ -57,3 +57,18 @@ def test_cursor_mirror_matches_the_oracle_protocol():
         assert np.array_equal(W[step], cur.write_pos), step
         assert oracle.commit(d, cur, slots, acc) == 0
         assert oracle.fold(d, ly, cur, slots) == 0
+
+
+def test_chunk_prefill_flops():
+    """One full 64-token chunk and a one-token tail, term by term: the Gram of
+    keys and queries against the keys, the state products of keys and queries,
+    the intra-chunk outputs, the state update."""
+    wl = bench.Workload(1)
+    K, V = wl.K, wl.V
+
+    def chunk(n):
+        return 2 * K * (2 * n) * n + 2 * V * K * (2 * n) + 2 * V * n * n + 2 * V * K * n
+
+    assert bench._prefill_chunk_flops(1, 65, wl) == (chunk(64) + chunk(1)) * wl.HV
+    assert bench._prefill_chunk_flops(3, 128, wl) == 3 * 2 * chunk(64) * wl.HV
+    assert bench._prefill_chunk_flops(2, 0, wl) == 0
