@@ -34,7 +34,9 @@
 //   * kind::tf32 MMAs with D from tensor memory add D W^T to Gam Q^ S^T (the
 //     outputs) and D (w K^) to the decayed state (the update).  The update's
 //     operands are split into tf32 high and low parts (three products), so the
-//     state keeps close to fp32 accuracy over long prompts.
+//     state keeps close to fp32 accuracy over long prompts;
+//   * a full chunk's outputs are staged over its (dead) v rows and written by
+//     one TMA store.
 // Tensor memory (512 columns, one CTA per SM): S 0..127, P_k 128..191,
 // P_q / outputs 192..255, Gram 256..319, D high 320..383, D low 384..447.
 #include <cuda.h>
@@ -103,7 +105,8 @@ __device__ __forceinline__ bool row_ok(const CursorArgs &C, int slot, int L, int
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_v, LayerArgs P, CursorArgs C,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  LayerArgs P, CursorArgs C,
                   const int32_t *__restrict__ slot_idx, int B, int N,
                   const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ bgate,
                   const float *__restrict__ A_log, const float *__restrict__ dt_bias,
@@ -144,6 +147,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             ptx::prefetch_tmap(&tm_k);
             ptx::prefetch_tmap(&tm_q);
             ptx::prefetch_tmap(&tm_v);
+            ptx::prefetch_tmap(&tm_o);
         }
     }
     if (warp == 0) ptx::tmem_alloc(sm_s + kOffMisc, kTmemCols);
@@ -203,6 +207,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         auto issue_chunk = [&](int buf, int tok0) {
             const uint32_t dst = sm_s + kOffRaw + buf * kRawBytes, bar = bar_full + 8 * buf;
             const int z = bb * N + tok0;
+            ptx::bulk_wait_read_all();   // an output store may still read this buffer's v rows
             ptx::mbar_expect_tx(bar, kRawBytes);
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
@@ -213,12 +218,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             inflight |= 1u << buf;
         };
         if (tid == 0 && nch > 0) issue_chunk(gbuf, 0);
-        // the gates' raw inputs of the first chunk (threads 0..63, one token each)
-        float ra = 0.0f, rb = 0.0f;
+        // the gates' raw inputs of the first chunk (threads 0..63, one token
+        // each), kept as bf16 bits: converted only when used, so that the
+        // loads stay in flight until then
+        const unsigned short *a16 = reinterpret_cast<const unsigned short *>(a);
+        const unsigned short *b16 = reinterpret_cast<const unsigned short *>(bgate);
+        uint32_t ra = 0u, rb = 0u;
         if (tid < kC && tid < N) {
             const size_t o = ((size_t)bb * N + tid) * HV + hv;
-            ra = __bfloat162float(a[o]);
-            rb = __bfloat162float(bgate[o]);
+            ra = a16[o];
+            rb = b16[o];
         }
 
         for (int c = 0; c < nch; ++c) {
@@ -231,15 +240,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (tid < kC) {
                 float g = 0.0f;
                 if (tid < n) {
-                    g = gate_g(Alog, ra, dtb);
-                    be = gate_beta(rb);
+                    g = gate_g(Alog, __uint_as_float(ra << 16), dtb);
+                    be = gate_beta(__uint_as_float(rb << 16));
                 }
                 const int tn = c0 + kC + tid;
-                ra = rb = 0.0f;
+                ra = rb = 0u;
                 if (tn < N) {
                     const size_t o = ((size_t)bb * N + tn) * HV + hv;
-                    ra = __bfloat162float(a[o]);
-                    rb = __bfloat162float(bgate[o]);
+                    ra = a16[o];
+                    rb = b16[o];
                 }
                 gsum = g;
 #pragma unroll
@@ -351,26 +360,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 const int t = row & (kC - 1), i0 = 32 * grp;
                 const float Gt = Gs[t];
                 const bool tv = t < n;
-                if (row < kC) {
-                    const float ft = betaS[t] * rn[t];
+                const bool keyrow = row < kC;
+                // key rows: A^T[i][t] = beta_t exp(G_t - G_i) <k^_t, k^_i> (i < t);
+                // query rows: W[t][i] = exp(G_t - G_i) <q^_t, k^_i> (i <= t)
+                const float ft = keyrow ? betaS[t] * rn[t] : rn[kC + t];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int i = i0 + e;
-                        AT[i * kALd + t] = (tv && i < t) ? ft * __expf(Gt - Gs[i]) * gr[e] * rn[i] : 0.0f;
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 g4 = *reinterpret_cast<const float4 *>(Gs + i0 + 4 * i4);
+                    const float4 n4 = *reinterpret_cast<const float4 *>(rn + i0 + 4 * i4);
+                    const float gi[4] = {g4.x, g4.y, g4.z, g4.w}, ni[4] = {n4.x, n4.y, n4.z, n4.w};
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = i0 + 4 * i4 + e;
+                        const float x = ft * __expf(Gt - gi[e]) * gr[4 * i4 + e] * ni[e];
+                        o[e] = (tv && (keyrow ? i < t : i <= t)) ? x : 0.0f;
                     }
-                } else {
-                    const float ft = rn[kC + t];
+                    if (keyrow) {
 #pragma unroll
-                    for (int i4 = 0; i4 < 8; ++i4) {
-                        float o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = i0 + 4 * i4 + e;
-                            o[e] = (tv && i <= t) ? ptx::round_tf32(ft * __expf(Gt - Gs[i]) * gr[4 * i4 + e] * rn[i])
-                                                  : 0.0f;
-                        }
+                        for (int e = 0; e < 4; ++e) AT[(i0 + 4 * i4 + e) * kALd + t] = o[e];
+                    } else {
                         *reinterpret_cast<float4 *>(sm + kOffW + sw_f32(kAtomW, t, i0 + 4 * i4)) =
-                            make_float4(o[0], o[1], o[2], o[3]);
+                            make_float4(ptx::round_tf32(o[0]), ptx::round_tf32(o[1]), ptx::round_tf32(o[2]),
+                                        ptx::round_tf32(o[3]));
                     }
                 }
             }
@@ -390,25 +402,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                         const int t = 16 * b + j;
                         r[j] = t < n ? betaS[t] * (__bfloat162float(vr[t * kBV + row]) - Gam[t] * r[j]) : 0.0f;
                     }
-#pragma unroll 2
-                    for (int i = 0; i < 16 * b; ++i) {
-                        const float x = Dsm[i * kBV + row];
-                        const float4 *ar = reinterpret_cast<const float4 *>(AT + i * kALd + 16 * b);
+                    {
+                        float2 r2[8];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 a4 = ar[q];
-                            r[4 * q] = fmaf(-a4.x, x, r[4 * q]);
-                            r[4 * q + 1] = fmaf(-a4.y, x, r[4 * q + 1]);
-                            r[4 * q + 2] = fmaf(-a4.z, x, r[4 * q + 2]);
-                            r[4 * q + 3] = fmaf(-a4.w, x, r[4 * q + 3]);
+                        for (int q = 0; q < 8; ++q) r2[q] = make_float2(r[2 * q], r[2 * q + 1]);
+#pragma unroll 4
+                        for (int i = 0; i < 16 * b; ++i) {
+                            const float x = -Dsm[i * kBV + row];
+                            const float2 x2 = make_float2(x, x);
+                            const float4 *ar = reinterpret_cast<const float4 *>(AT + i * kALd + 16 * b);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const float4 a4 = ar[q];
+                                r2[2 * q] = __ffma2_rn(make_float2(a4.x, a4.y), x2, r2[2 * q]);
+                                r2[2 * q + 1] = __ffma2_rn(make_float2(a4.z, a4.w), x2, r2[2 * q + 1]);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            r[2 * q] = r2[q].x;
+                            r[2 * q + 1] = r2[q].y;
                         }
                     }
 #pragma unroll
                     for (int i = 0; i < 15; ++i) {
                         const float x = r[i];
-                        const float *ar = AT + (16 * b + i) * kALd + 16 * b;
+                        const float4 *ar = reinterpret_cast<const float4 *>(AT + (16 * b + i) * kALd + 16 * b);
 #pragma unroll
-                        for (int j = i + 1; j < 16; ++j) r[j] = fmaf(-ar[j], x, r[j]);
+                        for (int q = (i + 1) / 4; q < 4; ++q) {
+                            const float4 a4 = ar[q];
+                            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (4 * q + e > i) r[4 * q + e] = fmaf(-av[e], x, r[4 * q + e]);
+                        }
                     }
                     if (b < kC / 16 - 1) {
 #pragma unroll
@@ -488,7 +515,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
             ptx::tc_fence_after_sync();
 
-            // ---- 8. the chunk's outputs of this state row, tokens 32 grp .. + 31
+            // ---- 8. the chunk's outputs of this state row, tokens 32 grp .. + 31:
+            //         a full chunk is staged over its (dead) v rows and leaves by
+            //         one TMA store; a ragged one is stored directly
+            const bool full = n == kC;
+            __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(sm + kOffRaw + buf * kRawBytes + 2 * kAtomKQ);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 float o16[16];
@@ -497,14 +528,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int t = 32 * grp + 16 * j + e;
-                    if (t < n)
-                        out[(((size_t)bb * N + c0 + t) * HV + hv) * V + v0 + row] = __float2bfloat16_rn(P.scale * o16[e]);
+                    const __nv_bfloat16 o = __float2bfloat16_rn(P.scale * o16[e]);
+                    if (full)
+                        stage[t * kBV + row] = o;
+                    else if (t < n)
+                        out[(((size_t)bb * N + c0 + t) * HV + hv) * V + v0 + row] = o;
                 }
             }
             // the buffer and the TMEM columns are reused by the next chunk
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
+            if (full && tid == 0) {
+                ptx::tma_store_3d(&tm_o, sm_s + kOffRaw + buf * kRawBytes + 2 * kAtomKQ, v0, hv, bb * N + c0);
+                ptx::bulk_commit_group();
+            }
             gbuf ^= 1;
         }
         if (dead) {
@@ -541,6 +579,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         __syncthreads();
     }
 
+    if (tid == 0) ptx::bulk_wait_all();   // the last output stores
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -627,16 +666,17 @@ cudaError_t launch_prefill_tc(const LayerArgs &P, const CursorArgs &C, const int
     if (grid <= 0) return cudaSuccess;
     EncodeTiledFnP enc = encode_fn_p();
     if (!enc) return cudaErrorNotSupported;
-    CUtensorMap mk{}, mq{}, mv{};   // N == 0: no copy is issued and the maps stay empty
+    CUtensorMap mk{}, mq{}, mv{}, mo{};   // N == 0: no copy is issued and the maps stay empty
     if (N > 0) {
         const long long tokens = (long long)B * N;
         if (!token_map(enc, &mk, k, P.K, P.H, tokens, 64, true) ||
             !token_map(enc, &mq, q, P.K, P.H, tokens, 64, true) ||
-            !token_map(enc, &mv, v, P.V, P.HV, tokens, ptc::kBV, false))
+            !token_map(enc, &mv, v, P.V, P.HV, tokens, ptc::kBV, false) ||
+            !token_map(enc, &mo, out, P.V, P.HV, tokens, ptc::kBV, false))
             return cudaErrorInvalidValue;
     }
     ptc::prefill_tc_kernel<<<grid, ptc::kThreads, ptc::kSmemBytes, stream>>>(
-        mk, mq, mv, P, C, slot_idx, B, N, static_cast<const __nv_bfloat16 *>(a),
+        mk, mq, mv, mo, P, C, slot_idx, B, N, static_cast<const __nv_bfloat16 *>(a),
         static_cast<const __nv_bfloat16 *>(b), A_log, dt_bias, static_cast<__nv_bfloat16 *>(out), from_zero,
         data_wait_limit());
     return cudaGetLastError();
