@@ -52,6 +52,9 @@ constexpr int kC = 64;          // tokens per chunk
 constexpr int kK = 128;         // key dim
 constexpr int kBV = 128;        // state rows per unit = MMA M
 constexpr int kThreads = 256;   // two groups of four warps
+// the thread that issues the chunk copies and output stores: outside the
+// warps that compute the gates (0, 1) and apart from the MMA issuer (0)
+constexpr int kCopier = 64;
 
 // Shared-memory map (bytes from a 1024-aligned base).
 constexpr int kAtomKQ = 128 * 128;                 // one 64-channel bf16 slice of [K; Q]
@@ -157,7 +160,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const uint32_t tmem = static_cast<uint32_t>(misc[0]);
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's lanes
     uint32_t ph_full = 0, ph_m1 = 0, ph_m2 = 0;   // phase bits (ph_full: bit per buffer)
-    uint32_t inflight = 0;                        // thread 0: buffers whose copy was not seen landed
+    uint32_t inflight = 0;                        // copier: buffers whose copy was not seen landed
     uint32_t pend = 0;                            // MMA barriers whose wait ran out (bit 0: m1, 1: m2)
     int gbuf = 0;                                 // buffer of the next chunk
     bool dead = false;                            // a wait ran out: remaining rows are only marked
@@ -217,7 +220,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             ptx::tma_load_3d(dst + 2 * kAtomKQ, &tm_v, bar, v0, hv, z);
             inflight |= 1u << buf;
         };
-        if (tid == 0 && nch > 0) issue_chunk(gbuf, 0);
+        if (tid == kCopier && nch > 0) issue_chunk(gbuf, 0);
         // the gates' raw inputs of the first chunk (threads 0..63, one token
         // each), kept as bf16 bits: converted only when used, so that the
         // loads stay in flight until then
@@ -233,7 +236,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         for (int c = 0; c < nch; ++c) {
             const int c0 = c * kC, n = N - c0 < kC ? N - c0 : kC;
             const int buf = gbuf;
-            if (tid == 0 && c + 1 < nch) issue_chunk(buf ^ 1, c0 + kC);
+            if (tid == kCopier && c + 1 < nch) issue_chunk(buf ^ 1, c0 + kC);
 
             // ---- 1. gates and their prefix sum; next chunk's raw gates
             float gsum = 0.0f, be = 0.0f;
@@ -269,7 +272,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             const bool landed = ptx::mbar_wait(bar_full + 8 * buf, (ph_full >> buf) & 1u, wait_limit);
             if (landed) {   // (a phase not seen complete stays the one to drain)
                 ph_full ^= 1u << buf;
-                if (tid == 0) inflight &= ~(1u << buf);
+                if (tid == kCopier) inflight &= ~(1u << buf);
             }
             if (__syncthreads_or(!landed)) {
                 dead = true;
@@ -539,7 +542,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
             __syncthreads();
-            if (full && tid == 0) {
+            if (full && tid == kCopier) {
                 ptx::tma_store_3d(&tm_o, sm_s + kOffRaw + buf * kRawBytes + 2 * kAtomKQ, v0, hv, bb * N + c0);
                 ptx::bulk_commit_group();
             }
@@ -552,6 +555,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             if (tid == 0) {
                 atomicOr(C.status, GDN_SPEC_ST_TIMEOUT);
                 C.is_flush[slot] = kFoldFailed;
+            }
+            if (tid == kCopier) {
                 for (int bf = 0; bf < 2; ++bf)
                     if (inflight & (1u << bf)) ptx::mbar_wait(bar_full + 8 * bf, (ph_full >> bf) & 1u);
                 inflight = 0;
@@ -579,7 +584,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         __syncthreads();
     }
 
-    if (tid == 0) ptx::bulk_wait_all();   // the last output stores
+    if (tid == kCopier) ptx::bulk_wait_all();   // the last output stores
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
