@@ -87,7 +87,8 @@ def kernel_source_hash(path_name: str = "tc") -> str:
     it includes), which keys the committed ncu traffic record."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_spec_gb300", "csrc")
-    for name in (f"verify_{path_name}.cu", "common.cuh", "ptx_sm100.cuh"):
+    src = {"tc_kda": "verify_kda.cu"}.get(path_name, f"verify_{path_name}.cu")
+    for name in (src, "common.cuh", "ptx_sm100.cuh"):
         h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
@@ -98,6 +99,9 @@ ARITH = {
     "tc": "fp32; the Gram and the checkpoint product on tensor cores with tf32 operands "
           "and fp32 accumulation",
     "generic": "fp32 on CUDA cores",
+    "tc_kda": "fp32; the per-channel-decayed key products off the diagonal blocks and the "
+              "checkpoint product on tensor cores with tf32 operands and fp32 accumulation; "
+              "the diagonal blocks and the solve on CUDA cores",
     "chunk": "fp32; the chunk's Gram (bf16 operands), the state products and the update (tf32 "
              "operands, the update split into high and low parts) on tensor cores with fp32 "
              "accumulation; the triangular solve on CUDA cores",

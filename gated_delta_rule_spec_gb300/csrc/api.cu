@@ -23,6 +23,10 @@ cudaError_t launch_verify_generic(const LayerArgs &P, const CursorArgs &C, bool 
                                   cudaStream_t stream);
 size_t verify_generic_smem_bytes(int K, int L, int T, bool kda);
 bool verify_tc_supported(const LayerArgs &P, bool kda, bool bf16);
+bool verify_kda_tc_supported(const LayerArgs &P, bool kda, bool bf16);
+cudaError_t launch_verify_kda_tc(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx, int B,
+                                 const void *q, const void *k, const void *v, const void *a, const void *b,
+                                 const float *A_log, const float *dt_bias, void *out, cudaStream_t stream);
 cudaError_t launch_verify_tc(const LayerArgs &P, const CursorArgs &C, const int32_t *slot_idx,
                              int B, const void *q, const void *k, const void *v, const void *a,
                              const void *b, const float *A_log, const float *dt_bias, void *out,
@@ -146,7 +150,8 @@ const char *gdn_spec_verify_path(const gdn_spec_layer *layer) {
     const LayerArgs P = layer_args(layer);
     const bool kda = layer->gate_kind == GDN_SPEC_GATE_PER_KEY;
     const bool bf16 = layer->io_dtype == GDN_SPEC_DTYPE_BF16;
-    return verify_tc_supported(P, kda, bf16) ? "tc" : "generic";
+    if (verify_tc_supported(P, kda, bf16)) return "tc";
+    return verify_kda_tc_supported(P, kda, bf16) ? "tc_kda" : "generic";
 }
 
 const char *gdn_spec_prefill_path(const gdn_spec_layer *layer) {
@@ -176,6 +181,8 @@ int gdn_spec_verify(const gdn_spec_layer *layer, const gdn_spec_cursors *cursors
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (verify_tc_supported(P, kda, bf16))
         return cuda_rc(launch_verify_tc(P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, st));
+    if (verify_kda_tc_supported(P, kda, bf16))
+        return cuda_rc(launch_verify_kda_tc(P, C, slot_idx, B, q, k, v, a, b, A_log, dt_bias, out, st));
     if (verify_generic_smem_bytes(P.K, P.L, P.T, kda) > kMaxSmem) return GDN_SPEC_EUNSUPPORTED;
     return cuda_rc(launch_verify_generic(P, C, kda, bf16, slot_idx, B, q, k, v, a, b, A_log,
                                          dt_bias, out, st));

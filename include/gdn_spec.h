@@ -70,7 +70,8 @@ extern "C" {
                                     3: adds gdn_spec_verify_d, gdn_spec_set_wait_limit, commit's
                                        cursor check and the poisoning of rows a fold or prefill
                                        could not finish;
-                                    4: adds gdn_spec_prefill_path and the chunk-parallel prefill */
+                                    4: adds gdn_spec_prefill_path, the chunk-parallel prefill and
+                                       the tensor-core KDA verify ("tc_kda") */
 
 /* host-side error codes (return values) */
 #define GDN_SPEC_OK            0
@@ -311,7 +312,8 @@ const char *gdn_spec_strerror(int code);
 int gdn_spec_abi_version(void);
 
 /* Name of the verify kernel gdn_spec_verify would launch for this layer
- * ("tc" = TMA + tcgen05 path, "generic" = CUDA-core path), or NULL if the
+ * ("tc" = TMA + tcgen05 path for the scalar gate, "tc_kda" = TMA + tcgen05
+ * path for the per-key gate, "generic" = CUDA-core path), or NULL if the
  * layer is invalid.  Host only; launches nothing. */
 const char *gdn_spec_verify_path(const gdn_spec_layer *layer);
 

@@ -74,7 +74,10 @@ def test_layer_descriptor_errors(lib, kw, want):
     (dict(V=256), b"tc"),
     (dict(T=8), b"tc"),
     (dict(T=1), b"tc"),                                     # decode
-    (dict(gate_kind=binding.GATE_PER_KEY), b"generic"),    # KDA
+    (dict(gate_kind=binding.GATE_PER_KEY), b"tc_kda"),     # KDA
+    (dict(gate_kind=binding.GATE_PER_KEY, T=8), b"tc_kda"),
+    (dict(gate_kind=binding.GATE_PER_KEY, K=64), b"generic"),
+    (dict(gate_kind=binding.GATE_PER_KEY, io_dtype=binding.DTYPE_FP32), b"generic"),
     (dict(io_dtype=binding.DTYPE_FP32), b"generic"),
     (dict(L=128), b"generic"),
     (dict(T=9, L=64), b"generic"),
