@@ -36,6 +36,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "ptx_sm100.cuh"
@@ -170,25 +171,60 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
 
         // ---- 1. raw key and query rows into X (two threads per row), their
         //         norms, the key side channel; per-channel gates into alpha;
-        //         beta; the window's values (side channel, V-term)
-        {
-            const int x = tid >> 1, half = tid & 1;
-            const bool is_key = x < n, is_q = x >= kQRow && x < kQRow + T;
-            const __nv_bfloat16 *src = nullptr;
-            if (x < W)
-                src = rawk + (sh_h * L + ring_pos(base, x, L)) * K;
-            else if (is_key)
-                src = k + (((size_t)bb * T + (x - W)) * H + h) * K;
-            else if (is_q)
-                src = q + (((size_t)bb * T + (x - kQRow)) * H + h) * K;
-            uint4 w4[8];
+        //         beta; the window's values (side channel, V-term).  Every
+        //         global load of the phase is issued before any is used.
+        const int x = tid >> 1, half = tid & 1;
+        const bool is_key = x < n, is_q = x >= kQRow && x < kQRow + T;
+        const __nv_bfloat16 *src = nullptr;
+        if (x < W)
+            src = rawk + (sh_h * L + ring_pos(base, x, L)) * K;
+        else if (is_key)
+            src = k + (((size_t)bb * T + (x - W)) * H + h) * K;
+        else if (is_q)
+            src = q + (((size_t)bb * T + (x - kQRow)) * H + h) * K;
+        uint4 w4[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) w4[c] = make_uint4(0u, 0u, 0u, 0u);
-            if (src) {
-                const uint4 *s4 = reinterpret_cast<const uint4 *>(src) + 8 * half;
+        for (int c = 0; c < 8; ++c) w4[c] = make_uint4(0u, 0u, 0u, 0u);
+        if (src) {
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(src) + 8 * half;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) w4[c] = s4[c];
+            for (int c = 0; c < 8; ++c) w4[c] = s4[c];
+        }
+        // gates: thread = (4 channels, tokens j0, j0 + 8, ...): the ring's g
+        // for history tokens, the raw a (element loads: a and dt_bias carry no
+        // alignment promise) for window tokens
+        const int c4 = 4 * (tid & 31), j0 = tid >> 5;
+        float4 gv[kLMax / 8];
+#pragma unroll
+        for (int m = 0; m < kLMax / 8; ++m) {
+            const int j = j0 + 8 * m;
+            gv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < W) {
+                gv[m] = *reinterpret_cast<const float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4);
+            } else if (j < n) {
+                const __nv_bfloat16 *ar = a + (((size_t)bb * T + (j - W)) * HV + hv) * K + c4;
+                gv[m] = make_float4(bf(ar), bf(ar + 1), bf(ar + 2), bf(ar + 3));
             }
+        }
+        float be_in = 0.0f;
+        if (tid < W)
+            be_in = P.ring_beta[sh_hv * L + ring_pos(base, tid, L)];
+        else if (tid < n)
+            be_in = bf(bgate + ((size_t)bb * T + (tid - W)) * HV + hv);
+        float vwin[kTMax];
+#pragma unroll
+        for (int s = 0; s < kTMax; ++s) vwin[s] = 0.0f;
+        __nv_bfloat16 vraw[kTMax];
+        if (grp == 1 && vrow < V) {
+#pragma unroll
+            for (int s = 0; s < kTMax; ++s)
+                if (s < T) vraw[s] = v[(((size_t)bb * T + s) * HV + hv) * V + vrow];
+        }
+        const float alog = A_log[hv];
+        const float4 dtb4 = make_float4(dt_bias[(size_t)hv * K + c4], dt_bias[(size_t)hv * K + c4 + 1],
+                                        dt_bias[(size_t)hv * K + c4 + 2], dt_bias[(size_t)hv * K + c4 + 3]);
+        // now use them
+        {
             float ss = 0.0f;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -212,90 +248,96 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
                 }
             }
         }
-        // alpha: thread = (4 channels, every eighth token)
-        {
-            const int c4 = 4 * (tid & 31);
-            const float alog = A_log[hv];
-            for (int j = tid >> 5; j < n; j += kThreads / 32) {
-                float g[4];
-                if (j < W) {
-                    const float4 g4 = *reinterpret_cast<const float4 *>(
-                        P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4);
-                    g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
-                } else {
-                    // (a and dt_bias carry no alignment promise: element loads)
-                    const size_t tk = (size_t)bb * T + (j - W);
-                    const __nv_bfloat16 *ar = a + (tk * HV + hv) * K + c4;
-                    const float *dr = dt_bias + (size_t)hv * K + c4;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) g[e] = gate_g(alog, bf(ar + e), dr[e]);
-                    if (vb == 0)
-                        *reinterpret_cast<float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4) =
-                            make_float4(g[0], g[1], g[2], g[3]);
-                }
-                *reinterpret_cast<float4 *>(al + j * K + c4) =
-                    make_float4(expf(g[0]), expf(g[1]), expf(g[2]), expf(g[3]));
+        for (int m = 0; m < kLMax / 8; ++m) {
+            const int j = j0 + 8 * m;
+            if (j >= n) continue;
+            float4 g = gv[m];
+            if (j >= W) {   // the window's gate, written to the ring (side channel)
+                g = make_float4(gate_g(alog, g.x, dtb4.x), gate_g(alog, g.y, dtb4.y), gate_g(alog, g.z, dtb4.z),
+                                gate_g(alog, g.w, dtb4.w));
+                if (vb == 0) *reinterpret_cast<float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4) = g;
             }
+            *reinterpret_cast<float4 *>(al + j * K + c4) = make_float4(expf(g.x), expf(g.y), expf(g.z), expf(g.w));
         }
         if (tid < n) {
-            float be;
-            const int pj = ring_pos(base, tid, L);
-            if (tid < W) {
-                be = P.ring_beta[sh_hv * L + pj];
-            } else {
-                be = gate_beta(bf(bgate + ((size_t)bb * T + (tid - W)) * HV + hv));
-                if (vb == 0) P.ring_beta[sh_hv * L + pj] = be;
+            float be = be_in;
+            if (tid >= W) {
+                be = gate_beta(be_in);
+                if (vb == 0) P.ring_beta[sh_hv * L + ring_pos(base, tid, L)] = be;
             }
             betaS[tid] = be;
         }
-        float vwin[kTMax];
-#pragma unroll
-        for (int s = 0; s < kTMax; ++s) vwin[s] = 0.0f;
         if (grp == 1 && vrow < V) {
 #pragma unroll
             for (int s = 0; s < kTMax; ++s)
                 if (s < T) {
-                    const __nv_bfloat16 x = v[(((size_t)bb * T + s) * HV + hv) * V + vrow];
-                    vwin[s] = __bfloat162float(x);
-                    rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = x;
+                    vwin[s] = __bfloat162float(vraw[s]);
+                    rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = vraw[s];
                 }
         }
         for (int i = tid; i < kLMax * kALd; i += kThreads) Am[i] = 0.0f;
         for (int i = tid; i < kLMax * kTMax; i += kThreads) Fm[i] = 0.0f;
         __syncthreads();
 
-        // ---- 2. the MMA operands: thread (channel c, group) walks the tokens
-        //         of its channel.  Group 0: L rows k^_x o Lin(p_x) (keys x < n,
-        //         queries at 64 + s with p = W + s); group 1: R_b rows
-        //         k^_r o Rin(r) o Mid(blk r, b) for every target block b > blk r
+        // ---- 2. the MMA operands, thread (channel c, group): L rows
+        //         k^_x o Lin(p_x) (keys x < n, queries at 64 + s with p = W + s)
+        //         and R_b rows k^_r o Rin(r) o Mid(blk r, b) for every target
+        //         block b > blk r.  Group 0 takes L and the source block 2,
+        //         group 1 the source blocks 0 and 1 (about the same number of
+        //         rows); the running products of different blocks are
+        //         independent chains, walked side by side.
         {
             const int c = row;
+            auto put_l = [&](int xr, float val) {
+                *reinterpret_cast<float *>(sm + kOffL + sw_f32(kAtomL, xr, c)) = ptx::round_tf32(val);
+            };
+            // R rows of source r in block bs: Mid(bs, bt) grows by block bt - 1
+            auto put_r = [&](int bs, int r, float val, float blk1, float blk2) {
+                for (int bt = bs + 1; bt <= nb; ++bt) {
+                    if (bt > bs + 1) val *= (bt == 2 ? blk1 : blk2);
+                    *reinterpret_cast<float *>(sm + kOffR + sw_f32(kAtomR, dcol(bt) + r, c)) = ptx::round_tf32(val);
+                }
+            };
             if (grp == 0) {
-                float lin = 1.0f;
-                for (int j = 0; j < n; ++j) {
-                    const float aj = al[j * K + c];
-                    lin = ((j & 15) == 0 ? 1.0f : lin) * aj;   // prod_{u = 16 blk(j) .. j}
-                    const float kx = bf(X + j * K + c) * rn[j];
-                    *reinterpret_cast<float *>(sm + kOffL + sw_f32(kAtomL, j, c)) = ptx::round_tf32(kx * lin);
-                    if (j >= W) {   // the query of window position s = j - W decays like token j
-                        const int xq = kQRow + (j - W);
-                        const float qx = bf(X + xq * K + c) * rn[xq];
-                        *reinterpret_cast<float *>(sm + kOffL + sw_f32(kAtomL, xq, c)) = ptx::round_tf32(qx * lin);
+                float lin[4] = {1.0f, 1.0f, 1.0f, 1.0f};   // prod_{u = 16 b .. j}
+#pragma unroll 2
+                for (int jj = 0; jj < 16; ++jj) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int j = 16 * b + jj;
+                        if (j < n) {
+                            lin[b] *= al[j * K + c];
+                            put_l(j, bf(X + j * K + c) * rn[j] * lin[b]);
+                            if (j >= W) {   // the query of window position j - W decays like token j
+                                const int xq = kQRow + (j - W);
+                                put_l(xq, bf(X + xq * K + c) * rn[xq] * lin[b]);
+                            }
+                        }
+                    }
+                }
+                if (nb >= 3) {
+                    float rin = 1.0f;   // prod_{u = r+1 .. 47}
+                    for (int r = 47; r >= 32; --r) {
+                        if (r < 47) rin *= al[(r + 1) * K + c];
+                        put_r(2, r, bf(X + r * K + c) * rn[r] * rin, 1.0f, 1.0f);
                     }
                 }
             } else if (nb >= 1) {
-                float blk[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-                for (int j = 0; j < 16 * nb; ++j) blk[j >> 4] *= al[j * K + c];
-                for (int bs = 0; bs < nb; ++bs) {
-                    float rin = 1.0f;   // prod_{u = r+1 .. 16 bs + 15}
-                    for (int r = 16 * bs + 15; r >= 16 * bs; --r) {
-                        if (r < 16 * bs + 15) rin *= al[(r + 1) * K + c];
-                        float val = bf(X + r * K + c) * rn[r] * rin;
-                        for (int bt = bs + 1; bt <= nb; ++bt) {   // Mid(bs, bt) grows by one block
-                            if (bt > bs + 1) val *= blk[bt - 1];
-                            const int rr = dcol(bt) + r;           // row of R_bt: its rows start at 16 bt (bt-1) / 2
-                            *reinterpret_cast<float *>(sm + kOffR + sw_f32(kAtomR, rr, c)) = ptx::round_tf32(val);
-                        }
+                float blk1 = 1.0f, blk2 = 1.0f;
+#pragma unroll 4
+                for (int jj = 0; jj < 16; ++jj) {
+                    if (nb >= 2) blk1 *= al[(16 + jj) * K + c];
+                    if (nb >= 3) blk2 *= al[(32 + jj) * K + c];
+                }
+                float rin0 = 1.0f, rin1 = 1.0f;   // prod_{u = r+1 .. 16 bs + 15}
+                for (int rr = 15; rr >= 0; --rr) {
+                    if (rr < 15) rin0 *= al[(rr + 1) * K + c];
+                    put_r(0, rr, bf(X + rr * K + c) * rn[rr] * rin0, blk1, blk2);
+                    if (nb >= 2) {
+                        const int r = 16 + rr;
+                        if (rr < 15) rin1 *= al[(r + 1) * K + c];
+                        put_r(1, r, bf(X + r * K + c) * rn[r] * rin1, blk1, blk2);
                     }
                 }
             }
@@ -359,44 +401,59 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
             }
             const int i0 = i & ~15;   // first token of i's block
             const float bi = live ? betaS[i] : 0.0f;
-            // the warp's eight rows share one block: the loop bound is warp-uniform
-            for (int r = (i | 15) - 1; r >= i0; --r) {
-                const bool act = live && r < i;
-                // z *= alpha_{r+1} for rows that have started (r < i); rows with
-                // r >= i wait with z = k^_i
-                float2 acc2 = make_float2(0.f, 0.f), accq2 = make_float2(0.f, 0.f);
+            // a warp's eight rows are consecutive tokens of one block: the
+            // steps run from the warp's last row down to the block's start
+            // (warp-uniform), and only warps holding a window row form zq
+            auto walk = [&](auto with_q) {
+                constexpr bool WQ = decltype(with_q)::value;
+                for (int r = (i | 7) - 1; r >= i0; --r) {
+                    const bool act = live && r < i;
+                    // z *= alpha_{r+1} for rows that have started (r < i); rows
+                    // with r >= i wait with z = k^_i
+                    float2 acc2 = make_float2(0.f, 0.f), accq2 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                    for (int m = 0; m < 4; ++m) {
 #pragma unroll
-                    for (int hlf = 0; hlf < 2; ++hlf) {
-                        const int ch = 8 * (part + 4 * m) + 4 * hlf;
-                        const float4 a4 = *reinterpret_cast<const float4 *>(al + (r + 1) * K + ch);
-                        const uint2 kr = *reinterpret_cast<const uint2 *>(X + r * K + ch);
-                        const float2 alo = act ? make_float2(a4.x, a4.y) : make_float2(1.f, 1.f);
-                        const float2 ahi = act ? make_float2(a4.z, a4.w) : make_float2(1.f, 1.f);
-                        const float2 klo = make_float2(__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xFFFF0000u));
-                        const float2 khi = make_float2(__uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xFFFF0000u));
-                        const int mi = 4 * m + 2 * hlf;
-                        z[mi] = __fmul2_rn(z[mi], alo);
-                        z[mi + 1] = __fmul2_rn(z[mi + 1], ahi);
-                        acc2 = __ffma2_rn(z[mi], klo, acc2);
-                        acc2 = __ffma2_rn(z[mi + 1], khi, acc2);
-                        zq[mi] = __fmul2_rn(zq[mi], alo);
-                        zq[mi + 1] = __fmul2_rn(zq[mi + 1], ahi);
-                        accq2 = __ffma2_rn(zq[mi], klo, accq2);
-                        accq2 = __ffma2_rn(zq[mi + 1], khi, accq2);
+                        for (int hlf = 0; hlf < 2; ++hlf) {
+                            const int ch = 8 * (part + 4 * m) + 4 * hlf;
+                            const float4 a4 = *reinterpret_cast<const float4 *>(al + (r + 1) * K + ch);
+                            const uint2 kr = *reinterpret_cast<const uint2 *>(X + r * K + ch);
+                            const float2 alo = act ? make_float2(a4.x, a4.y) : make_float2(1.f, 1.f);
+                            const float2 ahi = act ? make_float2(a4.z, a4.w) : make_float2(1.f, 1.f);
+                            const float2 klo = make_float2(__uint_as_float(kr.x << 16), __uint_as_float(kr.x & 0xFFFF0000u));
+                            const float2 khi = make_float2(__uint_as_float(kr.y << 16), __uint_as_float(kr.y & 0xFFFF0000u));
+                            const int mi = 4 * m + 2 * hlf;
+                            z[mi] = __fmul2_rn(z[mi], alo);
+                            z[mi + 1] = __fmul2_rn(z[mi + 1], ahi);
+                            acc2 = __ffma2_rn(z[mi], klo, acc2);
+                            acc2 = __ffma2_rn(z[mi + 1], khi, acc2);
+                            if (WQ) {
+                                zq[mi] = __fmul2_rn(zq[mi], alo);
+                                zq[mi + 1] = __fmul2_rn(zq[mi + 1], ahi);
+                                accq2 = __ffma2_rn(zq[mi], klo, accq2);
+                                accq2 = __ffma2_rn(zq[mi + 1], khi, accq2);
+                            }
+                        }
+                    }
+                    float acc = acc2.x + acc2.y;
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+                    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+                    float accq = 0.0f;
+                    if (WQ) {
+                        accq = accq2.x + accq2.y;
+                        accq += __shfl_xor_sync(0xffffffffu, accq, 1);
+                        accq += __shfl_xor_sync(0xffffffffu, accq, 2);
+                    }
+                    if (act && part == 0) {
+                        Am[i * kALd + r] = bi * acc * rn[r];
+                        if (WQ && win) Fm[r * kTMax + s] = accq * rn[r];
                     }
                 }
-                float acc = acc2.x + acc2.y, accq = accq2.x + accq2.y;
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                accq += __shfl_xor_sync(0xffffffffu, accq, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                accq += __shfl_xor_sync(0xffffffffu, accq, 2);
-                if (act && part == 0) {
-                    Am[i * kALd + r] = bi * acc * rn[r];
-                    if (win) Fm[r * kTMax + s] = accq * rn[r];
-                }
-            }
+            };
+            if (__any_sync(0xffffffffu, win))
+                walk(std::true_type{});
+            else
+                walk(std::false_type{});
         }
         // the off-diagonal blocks from TMEM: lane x is target row x (key i = x,
         // or query s = x - 64); its block's columns r < 16 blk(p)
