@@ -32,7 +32,8 @@ struct CursorArgs {
 // wait ran out); its cursor move then poisons the row (write_pos = -1).
 constexpr int kFoldFailed = 2;
 
-// Default iteration limit of a bounded mbarrier wait (about 0.3 s).
+// Default iteration limit of a bounded mbarrier wait (polls of at most about
+// 256 ns each: 0.3 s at most).
 constexpr uint32_t kWaitLimitDefault = 1u << 20;
 
 // Iteration limit of the first wait on each data copy (verify's checkpoint

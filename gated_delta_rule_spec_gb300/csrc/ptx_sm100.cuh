@@ -33,25 +33,25 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One poll of phase `parity`: the thread may be suspended for up to about
+// `hint_ns` while the phase is incomplete and resumes as soon as it completes.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred P1;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
         "selp.b32 %0, 1, 0, P1;\n\t}"
         : "=r"(done)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return done != 0;
 }
 
 // Bounded wait on phase `parity`; false if `limit` polls ran out (the
-// default, 2^20 polls, is about 0.3 s).
+// default, 2^20 polls of at most about 256 ns each, is about 0.3 s).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = 1u << 20) {
-    for (uint32_t it = 0; it < limit; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (it > 32) __nanosleep(256);
-    }
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try_wait(bar, parity, 256u)) return true;
     return false;
 }
 

@@ -292,7 +292,8 @@ int gdn_spec_snapshot_commit(const gdn_spec_layer *layer, const gdn_spec_cursors
  * drained with the default limit before its buffer is reused, so a small
  * limit exercises the timeout path without leaving anything in flight.
  * Applies to calls made (or graphs captured) afterwards, in every thread of
- * the process.  0xFFFFFFFF restores the default (2^20 polls, about 0.3 s).
+ * the process.  0xFFFFFFFF restores the default (2^20 polls of at most about
+ * 256 ns each: 0.3 s at most).
  * Returns the previous limit.  Not for production use.
  */
 uint32_t gdn_spec_set_wait_limit(uint32_t polls);
