@@ -157,3 +157,43 @@ def test_chunk_prefill_4096_tokens_without_decay():
     assert err <= OUT_TOL_BF16, err
     ck = c.check_state(slots)
     print(f"chunk prefill 4096 tokens, no decay: max-abs out {err:.2e}, ckpt rel-Fro {ck:.2e}")
+
+
+def test_chunk_prefill_bench_size_sampled_rows():
+    """The launch the bench times, B = 128 prompts of 256 tokens over a 512-slot
+    pool (Qwen3-Next heads, from zero): every row runs on the GPU, and four
+    sampled rows are checked against the oracle (rows are independent, so the
+    oracle runs on those rows alone)."""
+    H, HV, K, V, L, S = 16, 32, 128, 128, 64, 512
+    B, N = 128, 256
+    rng = gen.rng_for(7, "prefill-bench-size")
+    d = oracle.Dims(H=H, HV=HV, K=K, V=V, T=4, L=L, num_slots=S, per_key_gate=False, scale=0.9)
+    layer = binding.SpecLayer(H, HV, K, V, 4, L, S, io_dtype="bf16", scale=0.9)
+    cur = binding.SpecCursors(S)
+    A_log, dt_bias = gen.layer_params(rng, HV, K, False)
+    slots = gen.scattered_slots(rng, S, B)
+    w = gen.window_inputs(rng, B, N, H, HV, K, V, gen.BF16)
+    dev = {n: to_dev(x) for n, x in w.items()}
+    out = binding.prefill(layer, cur, to_dev(slots), dev["q"], dev["k"], dev["v"], dev["a"], dev["b"],
+                          torch.from_numpy(A_log).cuda(), torch.from_numpy(dt_bias).cuda(), from_zero=True)
+    assert binding.read_status(cur) == 0
+    got_out = gen.to_f64(to_host(out))
+    got_ck = to_host(layer.checkpoint).astype(np.float64)
+    sample = np.array([0, 37, 101, 127])
+    orc = oracle.Layer(d)
+    orc_cur = oracle.Cursors(S, np.zeros(S, np.int32), np.zeros(S, np.int32), np.zeros(S, np.int32))
+    f = {n: gen.to_f64(x)[sample] for n, x in w.items()}
+    o_orc, st = oracle.prefill(d, orc, orc_cur, slots[sample], f["q"], f["k"], f["v"], f["a"], f["b"],
+                               A_log.astype(np.float64), dt_bias.astype(np.float64), from_zero=True,
+                               nthreads=NTHREADS)
+    assert st == 0
+    err = float(np.max(np.abs(got_out[sample] - o_orc)))
+    assert err <= OUT_TOL_BF16, err
+    worst = 0.0
+    for s in slots[sample]:
+        ref = orc.checkpoint[s]
+        worst = max(worst, np.linalg.norm(got_ck[s] - ref) / np.linalg.norm(ref))
+    assert worst <= CKPT_REL_FRO, worst
+    wp = to_host(cur.write_pos)
+    assert not wp[slots].any()
+    print(f"chunk prefill B=128 N=256, 4 sampled rows: max-abs out {err:.2e}, ckpt rel-Fro {worst:.2e}")
