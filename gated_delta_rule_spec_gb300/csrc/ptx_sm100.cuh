@@ -270,11 +270,11 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// x rounded to the nearest tf32 value (ties away from zero), as fp32 bits.
+// x rounded to the nearest tf32 value (ties away from zero), as fp32 bits:
+// half a tf32 unit added to the magnitude bits, then the 13 low bits cleared
+// (finite x; integer operations instead of a conversion instruction)
 __device__ __forceinline__ float round_tf32(float x) {
-    uint32_t u;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
-    return __uint_as_float(u);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 }  // namespace ptx
