@@ -510,7 +510,35 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
                     f0[qq] = (sq < T && lane < n) ? Fm[lane * kTMax + sq] : 0.0f;
                     f1[qq] = (sq < T && lane + 32 < n) ? Fm[(lane + 32) * kTMax + sq] : 0.0f;
                 }
-                for (int j = n - 1; j >= 0; --j) {
+                // four tokens j-3..j per step: their 4 x 4 diagonal block is
+                // solved on every lane, then all lanes apply the four updates
+                // (which leave f[j-3..j] at their final values)
+                int j = n - 1;
+                for (; j >= 3; j -= 4) {
+                    float ar[4][2];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        ar[x][0] = Am[(j - x) * kALd + lane];
+                        ar[x][1] = Am[(j - x) * kALd + 32 + lane];
+                    }
+                    const float d0 = Am[j * kALd + j - 1], d1 = Am[j * kALd + j - 2], d2 = Am[j * kALd + j - 3];
+                    const float d3 = Am[(j - 1) * kALd + j - 2], d4 = Am[(j - 1) * kALd + j - 3];
+                    const float d5 = Am[(j - 2) * kALd + j - 3];
+#pragma unroll
+                    for (int qq = 0; qq < SPW; ++qq) {
+                        float fj[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            fj[x] = __shfl_sync(0xffffffffu, (j - x) < 32 ? f0[qq] : f1[qq], (j - x) & 31);
+                        const float m0 = fj[0];
+                        const float m1 = fmaf(-d0, m0, fj[1]);
+                        const float m2 = fmaf(-d3, m1, fmaf(-d1, m0, fj[2]));
+                        const float m3 = fmaf(-d5, m2, fmaf(-d4, m1, fmaf(-d2, m0, fj[3])));
+                        f0[qq] = fmaf(-ar[3][0], m3, fmaf(-ar[2][0], m2, fmaf(-ar[1][0], m1, fmaf(-ar[0][0], m0, f0[qq]))));
+                        f1[qq] = fmaf(-ar[3][1], m3, fmaf(-ar[2][1], m2, fmaf(-ar[1][1], m1, fmaf(-ar[0][1], m0, f1[qq]))));
+                    }
+                }
+                for (; j >= 0; --j) {
                     const float a0 = Am[j * kALd + lane], a1 = Am[j * kALd + 32 + lane];
 #pragma unroll
                     for (int qq = 0; qq < SPW; ++qq) {
