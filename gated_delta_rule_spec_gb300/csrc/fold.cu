@@ -9,14 +9,17 @@
 //     d  = beta_t (v_t - S k^_t),   S <- S + d k^_t^T
 //
 // Rows of S are independent under the recurrence (row i only sees v_t[i]).
-// A thread owns an eighth of the K columns of TWO state rows (rows p and
-// p + 16 of a 32-row block; a row's dot product takes three shuffles; at
-// K = 32 a quarter of the columns of rows p and p + 32 of a 64-row block), so
-// every key value it reads from shared memory serves both rows.  The keys
-// stay in shared memory as the raw I/O-dtype records (bf16: half the bytes
-// of fp32) and are widened in registers: reading the keys is what bounds the
-// replay, and the two choices together cut that traffic per state row by
-// four.  The elementwise work uses Blackwell's packed fp32x2 instructions.
+// A group of eight threads holds four state rows, each thread an eighth of
+// their K columns (at K = 32 four threads and a quarter), so every key value
+// it reads from shared memory serves four rows.  The four rows' dot products
+// are reduced over the group by a reduce-scatter: two shuffles split the
+// rows between the threads (each keeps two rows' sums, then one), a third
+// finishes the sum (at K = 32 the two splits do), each thread computes the
+// delta of the row it ends with,
+// and four shuffles hand the deltas to the group.  The keys stay in shared
+// memory as the raw I/O-dtype records (bf16: half the bytes of fp32) and are
+// widened in registers: per record and state row this reads 64 bytes of
+// keys.  The elementwise work uses Blackwell's packed fp32x2 instructions.
 //
 // With one gate per (token, v-head) the decay is carried as a running scalar
 // instead of being applied to every element: S = gam * R with gam the product
@@ -31,7 +34,7 @@
 // Only the rows whose is_flush is set do any work, and in steady state that
 // is a small share of the batch per step.  So the grid is persistent: every
 // CTA scans the batch's flags, builds the same compact list of slots to
-// fold, and takes work items (row, layer, v-head, block of 64 state rows)
+// fold, and takes work items (row, layer, v-head, block of 32 state rows)
 // round-robin from it.  An item's keys (one or two contiguous ring segments)
 // and values (one short run per record) arrive by bulk asynchronous copies
 // on an mbarrier while the CTA reads the gates and loads its state rows into
@@ -50,26 +53,26 @@
 
 namespace gdnspec {
 
-constexpr int kFoldThreads = 128;
+constexpr int kFoldThreads = 64;
 constexpr int kFoldMaxL = 128;                        // ring length limit of this kernel
 constexpr int kFoldScan = kFoldThreads;
 
-// Threads per pair of state rows: eight at K >= 64 (a pair's dot products
-// take three shuffles; 32 state rows per work item), four at K = 32 (two
-// shuffles; 64 rows per item).  Eight gives twice the items, which spreads a
-// step's few flagged rows over more SMs and more warps per SM.
+// Threads per group of four state rows: eight at K >= 64 (32 state rows per
+// work item of 64 threads), four at K = 32 (64 rows per item).  Small items
+// spread a step's few flagged rows over the SMs.
 template <int K>
 struct FoldGeom {
-    static constexpr int TPR = K >= 64 ? 8 : 4;
-    static constexpr int Pairs = kFoldThreads / TPR;
-    static constexpr int Rows = 2 * Pairs;            // state rows per work item
-    static constexpr int CtasPerSm = K >= 64 ? 6 : 4;
+    static constexpr int TPR = K >= 64 ? 8 : 4;       // threads per group of RPT rows
+    static constexpr int RPT = 4;                     // state rows per thread
+    static constexpr int Groups = kFoldThreads / TPR;
+    static constexpr int Rows = RPT * Groups;         // state rows per work item
+    static constexpr int CtasPerSm = 8;
 };
 
 __host__ __device__ constexpr size_t fold_pad16(size_t bytes) { return (bytes + 15) & ~(size_t)15; }
 
 // Shared memory of one item (every region starts on 16 bytes): raw keys
-// [L][K] and raw values [L][64 rows] in the I/O dtype, then fp32 (alpha,
+// [L][K] and raw values [L][rows of the item] in the I/O dtype, then fp32 (alpha,
 // 1/alpha) [L] (KDA: alpha [L][K]), beta [L], 1/|k| [L], and the compacted
 // slot list with its cursors.
 struct FoldSmem {
@@ -98,7 +101,8 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
     constexpr int kFoldTPR = FoldGeom<K>::TPR;
-    constexpr int kFoldPairs = FoldGeom<K>::Pairs;
+    constexpr int kGroups = FoldGeom<K>::Groups;
+    constexpr int kRPT = FoldGeom<K>::RPT;
     constexpr int kFoldRows = FoldGeom<K>::Rows;
     constexpr int kPer = KC::kVals;                 // key values per 16-byte chunk
     constexpr int kNC = K / kPer / kFoldTPR;        // chunks per thread: chunk part + TPR m
@@ -120,7 +124,14 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     const uint32_t bar = ptx::smem_addr(&s_bar);
     const int vblocks = (V + kFoldRows - 1) / kFoldRows;
     const int per_row = n_layers * HV * vblocks;
-    const int pair = tid / kFoldTPR, part = tid % kFoldTPR;
+    const int grp = tid / kFoldTPR, part = tid % kFoldTPR;
+    // the dot products of the group's four rows are reduced over its TPR
+    // threads by splitting on two bits of part (S1, S0): each thread ends with
+    // the full sum of row 2 h1 + h0 and computes that row's delta
+    constexpr int S1 = kFoldTPR == 8 ? 2 : 1, S0 = S1 - 1;
+    const int h1 = (part >> S1) & 1, h0 = (part >> S0) & 1;
+    const int own = 2 * h1 + h0;
+    const int lane_base = lane & ~(kFoldTPR - 1);
     long long item_base = 0;  // items enumerated in earlier scan passes
     uint32_t phase = 0;
     // set when a drain wait ran out too: copies may still land in the buffers,
@@ -210,7 +221,28 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                     ptx::bulk_copy_g2s(ptx::smem_addr(Xv + (size_t)j * kFoldRows),
                                        rawv + (sh_hv * L + ring_pos(base_e, j, L)) * V + row0, vbytes, bar);
             }
-            // ---- 2. gates (thread per record) and this thread's two state rows
+            // ---- 2. this thread's four state rows (loads issued first: their latency
+            //         overlaps the gate loads below and the copies)
+            float2 S[kRPT][kNP];
+#pragma unroll
+            for (int rr = 0; rr < kRPT; ++rr) {
+#pragma unroll
+                for (int i = 0; i < kNP; ++i) S[rr][i] = make_float2(0.f, 0.f);
+                if (grp + kGroups * rr < nrows) {
+                    const float *srow = ckpt + (sh_hv * V + row0 + grp + kGroups * rr) * K;
+#pragma unroll
+                    for (int m = 0; m < kNC; ++m) {
+                        const float4 *src = reinterpret_cast<const float4 *>(srow + (part + kFoldTPR * m) * kPer);
+#pragma unroll
+                        for (int q = 0; q < kPer / 4; ++q) {
+                            const float4 f = src[q];
+                            S[rr][m * (kPer / 2) + 2 * q] = make_float2(f.x, f.y);
+                            S[rr][m * (kPer / 2) + 2 * q + 1] = make_float2(f.z, f.w);
+                        }
+                    }
+                }
+            }
+            // ---- 2'. gates (thread per record); their loads are in flight with the state rows'
             for (int j = tid; j < W; j += kFoldThreads) {
                 const int p = ring_pos(base_e, j, L);
                 if (!KDA) {
@@ -223,26 +255,6 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                 for (int idx = tid; idx < W * K; idx += kFoldThreads) {
                     const int j = idx / K, kk = idx - j * K;
                     alpha[idx] = expf(ring_g[(sh_hv * L + ring_pos(base_e, j, L)) * K + kk]);
-                }
-            }
-            float2 S[2][kNP];
-            const bool valid0 = pair < nrows, valid1 = pair + kFoldPairs < nrows;
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-#pragma unroll
-                for (int i = 0; i < kNP; ++i) S[rr][i] = make_float2(0.f, 0.f);
-                if (rr ? valid1 : valid0) {
-                    const float *srow = ckpt + (sh_hv * V + row0 + pair + rr * kFoldPairs) * K;
-#pragma unroll
-                    for (int m = 0; m < kNC; ++m) {
-                        const float4 *src = reinterpret_cast<const float4 *>(srow + (part + kFoldTPR * m) * kPer);
-#pragma unroll
-                        for (int q = 0; q < kPer / 4; ++q) {
-                            const float4 f = src[q];
-                            S[rr][m * (kPer / 2) + 2 * q] = make_float2(f.x, f.y);
-                            S[rr][m * (kPer / 2) + 2 * q + 1] = make_float2(f.z, f.w);
-                        }
-                    }
                 }
             }
             // ---- 3. the copies land; 1 / |k_t| for every record (two threads each)
@@ -262,7 +274,8 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                 if (__syncthreads_or(!drained)) dead = true;
                 continue;
             }
-            // (the trip count is the same in every thread: the shuffle is warp-wide)
+            // 1 / |k_j| of the raw keys (two threads per record; the trip count
+            // is the same in every thread: the shuffle is warp-wide)
             for (int j0 = 0; j0 < W; j0 += kFoldThreads / 2) {
                 const int j = j0 + (tid >> 1);
                 float ss = 0.0f;
@@ -283,10 +296,9 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             __syncthreads();
 
             // ---- 4. replay (decay, then the delta against the decayed state)
-            float gam = 1.0f, inv = 1.0f;   // scalar gate: S = gam R (every thread holds the same values)
-            for (int t = 0; t < W; ++t) {
+            // this thread's chunks of key t, widened
+            auto load_key = [&](int t, float2 (&x)[kNP]) {
                 const uint4 *xk = reinterpret_cast<const uint4 *>(Xk + (size_t)t * K);
-                float2 x[kNP];
 #pragma unroll
                 for (int m = 0; m < kNC; ++m) {
                     float2 c2[kPer / 2];
@@ -294,6 +306,47 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
 #pragma unroll
                     for (int i = 0; i < kPer / 2; ++i) x[m * (kPer / 2) + i] = c2[i];
                 }
+            };
+            // S x for the group's four rows, reduced over the group's threads;
+            // returns the full dot product of this thread's own row.  The first
+            // split keeps rows 2 h1, 2 h1 + 1 and sends the other two, the
+            // second keeps row 2 h1 + h0; the remaining bits sum what is left.
+            auto dot_own = [&](const float2 (&x)[kNP]) {
+                float u[kRPT];
+#pragma unroll
+                for (int rr = 0; rr < kRPT; ++rr) {
+                    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                    for (int i = 0; i < kNP; ++i) acc[i & 1] = __ffma2_rn(S[rr][i], x[i], acc[i & 1]);
+                    const float2 a2 = __fadd2_rn(acc[0], acc[1]);
+                    u[rr] = a2.x + a2.y;
+                }
+                float k0 = h1 ? u[2] : u[0], k1 = h1 ? u[3] : u[1];
+                const float s0 = h1 ? u[0] : u[2], s1 = h1 ? u[1] : u[3];
+                k0 += __shfl_xor_sync(0xffffffffu, s0, 1 << S1);
+                k1 += __shfl_xor_sync(0xffffffffu, s1, 1 << S1);
+                float uo = h0 ? k1 : k0;
+                uo += __shfl_xor_sync(0xffffffffu, h0 ? k0 : k1, 1 << S0);
+#pragma unroll
+                for (int o = 1; o < (1 << S0); o <<= 1) uo += __shfl_xor_sync(0xffffffffu, uo, o);
+                return uo;
+            };
+            // S += d_rr x^T for the group's four rows, each row's delta from the
+            // thread that owns it
+            auto update = [&](float dow, const float2 (&x)[kNP]) {
+#pragma unroll
+                for (int rr = 0; rr < kRPT; ++rr) {
+                    const float d = __shfl_sync(0xffffffffu, dow, lane_base | ((rr >> 1) << S1) | ((rr & 1) << S0));
+                    const float2 d2 = make_float2(d, d);
+#pragma unroll
+                    for (int i = 0; i < kNP; ++i) S[rr][i] = __ffma2_rn(d2, x[i], S[rr][i]);
+                }
+            };
+            const IO *vown = Xv + grp + kGroups * own;
+            float gam = 1.0f, inv = 1.0f;   // scalar gate: S = gam R (every thread holds the same values)
+            for (int t = 0; t < W; ++t) {
+                float2 x[kNP];
+                load_key(t, x);
                 if (KDA) {
                     const float *al = alpha + (size_t)t * K;
 #pragma unroll
@@ -304,7 +357,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                             const float4 a = a4[q];
                             const int i = m * (kPer / 2) + 2 * q;
 #pragma unroll
-                            for (int rr = 0; rr < 2; ++rr) {
+                            for (int rr = 0; rr < kRPT; ++rr) {
                                 S[rr][i] = __fmul2_rn(S[rr][i], make_float2(a.x, a.y));
                                 S[rr][i + 1] = __fmul2_rn(S[rr][i + 1], make_float2(a.z, a.w));
                             }
@@ -317,47 +370,24 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
                     if (gam < 0x1p-32f) {   // the same branch in every thread
                         const float2 g2 = make_float2(gam, gam);
 #pragma unroll
-                        for (int i = 0; i < kNP; ++i) {
-                            S[0][i] = __fmul2_rn(S[0][i], g2);
-                            S[1][i] = __fmul2_rn(S[1][i], g2);
-                        }
+                        for (int rr = 0; rr < kRPT; ++rr)
+#pragma unroll
+                            for (int i = 0; i < kNP; ++i) S[rr][i] = __fmul2_rn(S[rr][i], g2);
                         gam = 1.0f;
                         inv = 1.0f;
                     }
                 }
-                float2 acc[2][2] = {{make_float2(0.f, 0.f), make_float2(0.f, 0.f)},
-                                    {make_float2(0.f, 0.f), make_float2(0.f, 0.f)}};
-#pragma unroll
-                for (int i = 0; i < kNP; ++i) {
-                    acc[0][i & 1] = __ffma2_rn(S[0][i], x[i], acc[0][i & 1]);
-                    acc[1][i & 1] = __ffma2_rn(S[1][i], x[i], acc[1][i & 1]);
-                }
-                float u0 = (acc[0][0].x + acc[0][0].y) + (acc[0][1].x + acc[0][1].y);
-                float u1 = (acc[1][0].x + acc[1][0].y) + (acc[1][1].x + acc[1][1].y);
-#pragma unroll
-                for (int o = 1; o < kFoldTPR; o <<= 1) {   // the pair's TPR threads
-                    u0 += __shfl_xor_sync(0xffffffffu, u0, o);
-                    u1 += __shfl_xor_sync(0xffffffffu, u1, o);
-                }
+                const float uo = dot_own(x);
                 const float rs = rsS[t], be = betaS[t];
-                const float v0 = to_f32<IO>(Xv[(size_t)t * kFoldRows + pair]);
-                const float v1 = to_f32<IO>(Xv[(size_t)t * kFoldRows + pair + kFoldPairs]);
                 // KDA: S itself (inv stays 1); scalar gate: R, with v_t / gam
-                const float d0 = be * (v0 * inv - rs * u0) * rs;
-                const float d1 = be * (v1 * inv - rs * u1) * rs;
-                const float2 d20 = make_float2(d0, d0), d21 = make_float2(d1, d1);
-#pragma unroll
-                for (int i = 0; i < kNP; ++i) {
-                    S[0][i] = __ffma2_rn(d20, x[i], S[0][i]);
-                    S[1][i] = __ffma2_rn(d21, x[i], S[1][i]);
-                }
+                update(be * (to_f32<IO>(vown[(size_t)t * kFoldRows]) * inv - rs * uo) * rs, x);
             }
             // ---- 5. S = gam R back into the checkpoint
             const float2 g2 = make_float2(gam, gam);
 #pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                if (!(rr ? valid1 : valid0)) continue;
-                float *drow = ckpt + (sh_hv * V + row0 + pair + rr * kFoldPairs) * K;
+            for (int rr = 0; rr < kRPT; ++rr) {
+                if (grp + kGroups * rr >= nrows) continue;
+                float *drow = ckpt + (sh_hv * V + row0 + grp + kGroups * rr) * K;
 #pragma unroll
                 for (int m = 0; m < kNC; ++m) {
                     float4 *dst = reinterpret_cast<float4 *>(drow + (part + kFoldTPR * m) * kPer);
