@@ -53,20 +53,22 @@
 
 namespace gdnspec {
 
-constexpr int kFoldThreads = 64;
 constexpr int kFoldMaxL = 128;                        // ring length limit of this kernel
-constexpr int kFoldScan = kFoldThreads;
 
-// Threads per group of four state rows: eight at K >= 64 (32 state rows per
-// work item of 64 threads), four at K = 32 (64 rows per item).  Small items
-// spread a step's few flagged rows over the SMs.
-template <int K>
+// Threads per group of four state rows: eight at K >= 64, four at K = 32.
+// An item has 64 threads with one gate per (token, v-head): 32 state rows at
+// K >= 64 (small items spread a step's few flagged rows over the SMs); with
+// per-channel decays 128 threads and 64 rows, so that the item's fp32 decay
+// table [L][K] serves twice the rows and a step's items fit on the SMs at
+// once.  The flag scan takes one batch row per thread.
+template <int K, bool KDA>
 struct FoldGeom {
-    static constexpr int TPR = K >= 64 ? 8 : 4;       // threads per group of RPT rows
+    static constexpr int Threads = KDA ? 128 : 64;
+    static constexpr int TPR = K >= 64 ? 8 : 4;
     static constexpr int RPT = 4;                     // state rows per thread
-    static constexpr int Groups = kFoldThreads / TPR;
+    static constexpr int Groups = Threads / TPR;
     static constexpr int Rows = RPT * Groups;         // state rows per work item
-    static constexpr int CtasPerSm = 8;
+    static constexpr int CtasPerSm = KDA ? 4 : 8;
 };
 
 __host__ __device__ constexpr size_t fold_pad16(size_t bytes) { return (bytes + 15) & ~(size_t)15; }
@@ -78,15 +80,17 @@ __host__ __device__ constexpr size_t fold_pad16(size_t bytes) { return (bytes + 
 struct FoldSmem {
     size_t keys, vals, alpha, beta, rs, rows, meta, total;
     __host__ __device__ FoldSmem(int K, int L, bool kda, size_t io) {
-        const int item_rows = K >= 64 ? FoldGeom<128>::Rows : FoldGeom<32>::Rows;
+        const int item_rows = K >= 64 ? (kda ? FoldGeom<128, true>::Rows : FoldGeom<128, false>::Rows)
+                                      : (kda ? FoldGeom<32, true>::Rows : FoldGeom<32, false>::Rows);
+        const int scan = kda ? FoldGeom<128, true>::Threads : FoldGeom<128, false>::Threads;
         keys = 0;
         vals = keys + fold_pad16((size_t)L * K * io);
         alpha = vals + fold_pad16((size_t)L * item_rows * io);
         beta = alpha + fold_pad16(sizeof(float) * (size_t)L * (kda ? K : 2));
         rs = beta + fold_pad16(sizeof(float) * L);
         rows = rs + fold_pad16(sizeof(float) * L);
-        meta = rows + sizeof(int) * kFoldScan;
-        total = meta + sizeof(int) * kFoldScan;
+        meta = rows + sizeof(int) * scan;
+        total = meta + sizeof(int) * scan;
     }
 };
 
@@ -95,15 +99,17 @@ size_t fold_smem_bytes(int K, int L, bool kda, bool bf16) {
 }
 
 template <typename IO, bool KDA, int K>
-__global__ void __launch_bounds__(kFoldThreads, FoldGeom<K>::CtasPerSm)
+__global__ void __launch_bounds__(FoldGeom<K, KDA>::Threads, FoldGeom<K, KDA>::CtasPerSm)
 fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
             const int32_t *__restrict__ slot_idx, int B, uint32_t wait_limit) {
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
-    constexpr int kFoldTPR = FoldGeom<K>::TPR;
-    constexpr int kGroups = FoldGeom<K>::Groups;
-    constexpr int kRPT = FoldGeom<K>::RPT;
-    constexpr int kFoldRows = FoldGeom<K>::Rows;
+    constexpr int kFoldThreads = FoldGeom<K, KDA>::Threads;
+    constexpr int kFoldScan = kFoldThreads;
+    constexpr int kFoldTPR = FoldGeom<K, KDA>::TPR;
+    constexpr int kGroups = FoldGeom<K, KDA>::Groups;
+    constexpr int kRPT = FoldGeom<K, KDA>::RPT;
+    constexpr int kFoldRows = FoldGeom<K, KDA>::Rows;
     constexpr int kPer = KC::kVals;                 // key values per 16-byte chunk
     constexpr int kNC = K / kPer / kFoldTPR;        // chunks per thread: chunk part + TPR m
     constexpr int kNP = kNC * kPer / 2;             // float2 pairs per thread and row
@@ -421,8 +427,8 @@ static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n
     if (e != cudaSuccess) return e;
     // enough CTAs for every item of a typical step to run at once; the ones
     // without an item leave after the flag scan
-    kern<<<FoldGeom<K>::CtasPerSm * sms, kFoldThreads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B,
-                                                                        data_wait_limit());
+    using FG = FoldGeom<K, KDA>;
+    kern<<<FG::CtasPerSm * sms, FG::Threads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B, data_wait_limit());
     return cudaGetLastError();
 }
 
