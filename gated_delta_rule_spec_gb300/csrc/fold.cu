@@ -48,6 +48,7 @@
 // instead of moving it, since some of its layers and v-heads may be folded
 // and others not.
 #include "common.cuh"
+#include "launch_setup.cuh"
 #include "ptx_sm100.cuh"
 #include "replay.cuh"
 
@@ -418,12 +419,10 @@ static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n
                                  const CursorArgs &C, const int32_t *slot_idx, int B,
                                  cudaStream_t stream) {
     const size_t smem = FoldSmem(K, P.L, KDA, sizeof(IO)).total;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     auto kern = fold_kernel<IO, KDA, K>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static KernelSetup setup;
+    int sms = 0;
+    cudaError_t e = kernel_setup(setup, reinterpret_cast<const void *>(kern), smem, &sms);
     if (e != cudaSuccess) return e;
     // enough CTAs for every item of a typical step to run at once; the ones
     // without an item leave after the flag scan

@@ -27,6 +27,7 @@
 // v-head)); the checkpoint is only read and no cursor is touched.  Its commit
 // copies the state after the accepted tokens back into the checkpoint.
 #include "common.cuh"
+#include "launch_setup.cuh"
 #include "ptx_sm100.cuh"
 #include "replay.cuh"
 
@@ -451,12 +452,10 @@ static cudaError_t launch_prefill_k(const LayerArgs &P, const CursorArgs &C, con
                                     const float *dt_bias, void *out, int from_zero, float *snap,
                                     cudaStream_t stream) {
     const size_t smem = PrefillSmem(K, KDA, sizeof(IO)).total;
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     auto kern = prefill_kernel<IO, KDA, K, SNAP>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static KernelSetup setup;
+    int sms = 0;
+    cudaError_t e = kernel_setup(setup, reinterpret_cast<const void *>(kern), smem, &sms);
     if (e != cudaSuccess) return e;
     const long long items = (long long)B * P.HV * ((P.V + kPreRows - 1) / kPreRows);
     const long long cap = (long long)kPreCtasPerSm * sms;

@@ -32,6 +32,7 @@
 // and beta computed here.  rawk is written by one CTA per k-head (hv % G == 0,
 // V-block 0), g and beta by V-block 0 (sglang PR #36821 ring-write placement).
 #include "common.cuh"
+#include "launch_setup.cuh"
 #include "ptx_sm100.cuh"
 
 namespace gdnspec {
@@ -426,8 +427,9 @@ static cudaError_t launch_one(const LayerArgs &P, const CursorArgs &C, const int
                               cudaStream_t stream) {
     const size_t smem = verify_generic_smem_bytes(P.K, P.L, P.T, KDA);
     auto kern = verify_generic_kernel<IO, KDA>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    static KernelSetup setup;
+    int sms = 0;
+    cudaError_t e = kernel_setup(setup, reinterpret_cast<const void *>(kern), smem, &sms);
     if (e != cudaSuccess) return e;
     dim3 grid((P.V + kGenThreads - 1) / kGenThreads, B, P.HV);
     kern<<<grid, kGenThreads, smem, stream>>>(
