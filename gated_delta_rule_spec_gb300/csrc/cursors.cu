@@ -3,6 +3,7 @@
 // device so the whole decode step stays capturable in a CUDA graph (blog post
 // on sglang PR #28695, §1.3 and appendix A.2).
 #include "common.cuh"
+#include "launch_setup.cuh"
 
 namespace gdnspec {
 
@@ -13,6 +14,8 @@ constexpr int kCursorThreads = 256;
 // outside [0, L), as row_cursor_ok rejects them) is skipped with CURSOR_CORRUPT.
 __global__ void commit_kernel(CursorArgs C, int T, int L, const int32_t *__restrict__ slot_idx,
                               int B, const int32_t *__restrict__ accept_len) {
+    grid_dep_wait();   // the verify that read these cursors
+    grid_dep_launch();
     for (int bb = blockIdx.x * blockDim.x + threadIdx.x; bb < B; bb += gridDim.x * blockDim.x) {
         const int slot = slot_idx[bb];
         if (slot < 0) continue;
@@ -36,6 +39,8 @@ __global__ void commit_kernel(CursorArgs C, int T, int L, const int32_t *__restr
 // is_flush = kFoldFailed) is poisoned instead: write_pos = -1, so that every
 // later call reports CURSOR_CORRUPT for it until gdn_spec_reset.
 __global__ void fold_cursor_kernel(CursorArgs C, int L, const int32_t *__restrict__ slot_idx, int B) {
+    grid_dep_wait();   // the fold that read these cursors
+    grid_dep_launch();
     for (int bb = blockIdx.x * blockDim.x + threadIdx.x; bb < B; bb += gridDim.x * blockDim.x) {
         const int slot = slot_idx[bb];
         if (slot < 0) continue;
@@ -77,14 +82,14 @@ static int cursor_blocks(int B) {
 
 cudaError_t launch_commit(const CursorArgs &C, int T, int L, const int32_t *slot_idx, int B,
                           const int32_t *accept_len, cudaStream_t stream) {
-    commit_kernel<<<cursor_blocks(B), kCursorThreads, 0, stream>>>(C, T, L, slot_idx, B, accept_len);
-    return cudaGetLastError();
+    return launch_dependent(commit_kernel, dim3(cursor_blocks(B)), dim3(kCursorThreads), 0, stream, C, T, L,
+                            slot_idx, B, accept_len);
 }
 
 cudaError_t launch_fold_cursors(const CursorArgs &C, int L, const int32_t *slot_idx, int B,
                                 cudaStream_t stream) {
-    fold_cursor_kernel<<<cursor_blocks(B), kCursorThreads, 0, stream>>>(C, L, slot_idx, B);
-    return cudaGetLastError();
+    return launch_dependent(fold_cursor_kernel, dim3(cursor_blocks(B)), dim3(kCursorThreads), 0, stream, C, L,
+                            slot_idx, B);
 }
 
 cudaError_t launch_reset(const CursorArgs &C, const int32_t *slot_idx, int B, cudaStream_t stream) {

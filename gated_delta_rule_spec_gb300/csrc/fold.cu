@@ -149,6 +149,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
         ptx::mbar_init(bar, 1);
         ptx::mbar_init_fence();
     }
+    grid_dep_wait();   // the commit's flags and cursors (the cursor move starts as this grid exits)
     __syncthreads();
 
     for (int b0 = 0; b0 < B; b0 += kFoldScan) {
@@ -427,8 +428,8 @@ static cudaError_t launch_fold_k(const LayerArgs &P, const FoldLayers &FL, int n
     // enough CTAs for every item of a typical step to run at once; the ones
     // without an item leave after the flag scan
     using FG = FoldGeom<K, KDA>;
-    kern<<<FG::CtasPerSm * sms, FG::Threads, smem, stream>>>(P, FL, n_layers, C, slot_idx, B, data_wait_limit());
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(FG::CtasPerSm * sms), dim3(FG::Threads), smem, stream, P, FL, n_layers, C,
+                            slot_idx, B, data_wait_limit());
 }
 
 template <typename IO, bool KDA>

@@ -42,4 +42,31 @@ inline cudaError_t kernel_setup(KernelSetup &ks, const void *kern, size_t smem, 
     return cudaSuccess;
 }
 
+// Programmatic dependent launch, for the short kernels that follow one
+// another in a step (commit, fold, cursor move): such a kernel may start while
+// the kernel before it in the stream is finishing, and calls grid_dep_wait()
+// before its first global memory access (it returns once every grid the
+// kernel depends on has completed and its memory is visible; at once for a
+// kernel launched without the attribute).  grid_dep_launch() lets the next
+// kernel start its own launch early; only the commit and the cursor move call
+// it, right after their wait, so at most two neighbouring kernels overlap.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args &&...args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 }  // namespace gdnspec
