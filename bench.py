@@ -20,8 +20,8 @@ verify (an event node between kernels costs the step a few microseconds), so
 the verify kernel's own duration is measured in the timed region.  The
 checkpoint working set (B x 32 x 64 KiB = 256 MiB at B=128) exceeds L2.
 
---impl reference times the fp64 CPU oracle (the reference arm of this build)
-on a bounded sample of the same workload.
+--impl reference times the fp64 CPU oracle (the reference arm: the oracle
+itself on the host cores) on a bounded sample of the same workload.
 """
 from __future__ import annotations
 

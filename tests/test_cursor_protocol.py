@@ -5,7 +5,7 @@ The pages' own protocol ("A", the blog post on PR #28695, §4.4, §8.1 and
     if is_flush: cache_base = (cache_base + write_pos) & (L-1); write_pos = acc
     else:        write_pos += acc
     is_flush = (write_pos + 2T > L)
-This build calls the fold as its own step between commit and the next verify
+The library calls the fold as its own step between commit and the next verify
 (protocol "B"): commit does write_pos += acc and sets is_flush the same way;
 fold moves cache_base by write_pos and clears write_pos and is_flush.
 

@@ -7,8 +7,8 @@ per step, with the state carried in tensor memory.  These cases span many
 chunks and ragged tails, two 128-row blocks of V, grouped heads, raw
 (non-unit) keys and queries, decays from nearly none to underflowing, a
 continuation from the checkpoint, the empty prompt, and a wait that runs out.
-The bars are the spec ones: outputs within 3e-2 max-abs (bf16), the
-checkpoint within 1e-3 relative Frobenius.
+The bars are the path's stated tolerances: outputs within 3e-2 max-abs (bf16),
+the checkpoint within 1e-3 relative Frobenius.
 """
 import numpy as np
 import pytest
