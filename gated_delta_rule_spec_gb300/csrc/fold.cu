@@ -61,7 +61,9 @@ constexpr int kFoldMaxL = 128;                        // ring length limit of th
 // K >= 64 (small items spread a step's few flagged rows over the SMs); with
 // per-channel decays 128 threads and 64 rows, so that the item's fp32 decay
 // table [L][K] serves twice the rows and a step's items fit on the SMs at
-// once.  The flag scan takes one batch row per thread.
+// once.  The flag scan takes kFoldScanPer batch rows per thread.
+constexpr int kFoldScanPer = 4;   // batch rows per thread and flag-scan pass
+
 template <int K, bool KDA>
 struct FoldGeom {
     static constexpr int Threads = KDA ? 128 : 64;
@@ -83,7 +85,7 @@ struct FoldSmem {
     __host__ __device__ FoldSmem(int K, int L, bool kda, size_t io) {
         const int item_rows = K >= 64 ? (kda ? FoldGeom<128, true>::Rows : FoldGeom<128, false>::Rows)
                                       : (kda ? FoldGeom<32, true>::Rows : FoldGeom<32, false>::Rows);
-        const int scan = kda ? FoldGeom<128, true>::Threads : FoldGeom<128, false>::Threads;
+        const int scan = kFoldScanPer * (kda ? FoldGeom<128, true>::Threads : FoldGeom<128, false>::Threads);
         keys = 0;
         vals = keys + fold_pad16((size_t)L * K * io);
         alpha = vals + fold_pad16((size_t)L * item_rows * io);
@@ -106,7 +108,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     static_assert(K % 32 == 0 && K <= 128, "whole 16-byte key chunks per thread");
     using KC = KeyChunk<IO>;
     constexpr int kFoldThreads = FoldGeom<K, KDA>::Threads;
-    constexpr int kFoldScan = kFoldThreads;
+    constexpr int kFoldScan = kFoldScanPer * kFoldThreads;   // batch rows per scan pass
     constexpr int kFoldTPR = FoldGeom<K, KDA>::TPR;
     constexpr int kGroups = FoldGeom<K, KDA>::Groups;
     constexpr int kRPT = FoldGeom<K, KDA>::RPT;
@@ -116,7 +118,7 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     constexpr int kNP = kNC * kPer / 2;             // float2 pairs per thread and row
     static_assert(kNC >= 1, "at least one chunk per thread");
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ int s_count, s_warp_off[kFoldThreads / 32];
+    __shared__ int s_count, s_warp_off[kFoldScanPer][kFoldThreads / 32];
     __shared__ __align__(8) uint64_t s_bar;
     const int V = P.V, L = P.L, HV = P.HV, H = P.H;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -153,35 +155,50 @@ fold_kernel(LayerArgs P, FoldLayers FL, int n_layers, CursorArgs C,
     __syncthreads();
 
     for (int b0 = 0; b0 < B; b0 += kFoldScan) {
-        // ---- scan kFoldScan batch rows, compact the flagged ones (same list in every CTA)
-        const int bb = b0 + tid;
-        int flag = 0, wp = 0, base = 0, slot = -1;
-        if (bb < B) {
-            slot = slot_idx[bb];
-            if (slot >= 0 && slot < C.num_slots && C.is_flush[slot]) {
-                wp = C.write_pos[slot];
-                base = C.cache_base[slot];
-                flag = (wp > 0 && wp <= L && base >= 0 && base < L) ? 1 : 0;
+        // ---- scan kFoldScan batch rows, compact the flagged ones (same list in
+        //      every CTA, ordered by (k, warp, lane)); a row's flag and cursors
+        //      are read together, every load of the pass before any is used
+        int slot[kFoldScanPer], fl[kFoldScanPer], wp[kFoldScanPer], base[kFoldScanPer];
+#pragma unroll
+        for (int k = 0; k < kFoldScanPer; ++k) {
+            const int bb = b0 + k * kFoldThreads + tid;
+            slot[k] = bb < B ? slot_idx[bb] : -1;
+        }
+#pragma unroll
+        for (int k = 0; k < kFoldScanPer; ++k) {
+            fl[k] = wp[k] = base[k] = 0;
+            if (slot[k] >= 0 && slot[k] < C.num_slots) {
+                fl[k] = C.is_flush[slot[k]];
+                wp[k] = C.write_pos[slot[k]];
+                base[k] = C.cache_base[slot[k]];
             }
         }
-        const unsigned ball = __ballot_sync(0xffffffffu, flag);
-        if (lane == 0) s_warp_off[warp] = __popc(ball);
+        unsigned ball[kFoldScanPer];
+#pragma unroll
+        for (int k = 0; k < kFoldScanPer; ++k) {
+            fl[k] = (fl[k] && wp[k] > 0 && wp[k] <= L && base[k] >= 0 && base[k] < L) ? 1 : 0;
+            ball[k] = __ballot_sync(0xffffffffu, fl[k]);
+            if (lane == 0) s_warp_off[k][warp] = __popc(ball[k]);
+        }
         __syncthreads();
         if (tid == 0) {
             int acc = 0;
-            for (int w = 0; w < kFoldThreads / 32; ++w) {
-                const int c = s_warp_off[w];
-                s_warp_off[w] = acc;
-                acc += c;
-            }
+            for (int k = 0; k < kFoldScanPer; ++k)
+                for (int w = 0; w < kFoldThreads / 32; ++w) {
+                    const int c = s_warp_off[k][w];
+                    s_warp_off[k][w] = acc;
+                    acc += c;
+                }
             s_count = acc;
         }
         __syncthreads();
-        if (flag) {
-            const int pos = s_warp_off[warp] + __popc(ball & ((1u << lane) - 1u));
-            rows[pos] = slot;
-            meta[pos] = (wp << 16) | base;
-        }
+#pragma unroll
+        for (int k = 0; k < kFoldScanPer; ++k)
+            if (fl[k]) {
+                const int pos = s_warp_off[k][warp] + __popc(ball[k] & ((1u << lane) - 1u));
+                rows[pos] = slot[k];
+                meta[pos] = (wp[k] << 16) | base[k];
+            }
         __syncthreads();
         const long long nitems = (long long)s_count * per_row;
 
