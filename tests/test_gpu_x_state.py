@@ -10,6 +10,7 @@
 * Bitwise "untouched": verify leaves every checkpoint and the cursors as they
   were; fold leaves the checkpoint of every slot it did not fold as it was;
   commit skips rows with corrupt cursors and reports them.
+* A fold over more batch rows than its flag scan takes in one pass.
 
 All through the C ABI.  Bars as elsewhere: outputs max-abs <= 3e-2 (bf16 I/O),
 each folded (slot, v-head) checkpoint within 1e-3 relative Frobenius error,
@@ -204,3 +205,27 @@ def test_commit_rejects_corrupt_cursors_like_the_oracle():
     assert st == oracle.ST_CURSOR_CORRUPT
     assert binding.read_status(sc.cur) == st
     sc.check_cursors()
+
+
+def test_fold_more_rows_than_one_scan_pass():
+    """B = 300 rows, more than the fold's flag scan takes in one pass (256 rows
+    with the scalar gate): rows of both passes are flagged and folded in the
+    same launch.  L = 16, so most rows fold every few rounds; cursors bit-exact
+    after every call, every used slot's checkpoint within the bar."""
+    wl = gen.Workload("fold-300", B=300, H=1, HV=2, K=128, V=128, T=4, L=16, prefix=8)
+    sc = Scenario(wl, B=300, seed=81, num_slots=320, random_cursors=True)
+    assert binding.verify_path(sc.layer) == "tc"
+    folded_late = 0
+    for r in range(6):
+        out, o_orc, st = sc.verify(sc.window())
+        assert st == 0 and sc.out_error(out, o_orc) <= sc.out_tol(), f"round {r}"
+        acc = gen.accept_lens(sc.rng, sc.B, wl.T, full_frac=0.6)
+        assert sc.commit(acc) == 0
+        sc.check_cursors()
+        flagged_rows = [i for i, s in enumerate(sc.slot_idx) if s >= 0 and sc.orc_cur.is_flush[s]]
+        folded_late += sum(1 for i in flagged_rows if i >= 256)
+        assert sc.fold() == 0
+        sc.check_cursors()
+    assert folded_late > 0
+    used = sorted(set(int(s) for s in sc.slot_idx if s >= 0))
+    assert sc.ckpt_error_per_slot(used) <= CKPT_REL_FRO
