@@ -2,8 +2,9 @@
 // prhub summary of sglang PR #36821) on sm_103a: TMA + tcgen05.
 //
 // Shapes: bf16 I/O, per-key gate, K = 128, V a multiple of 128, ring L <= 64,
-// window T <= 8.  A unit is (batch row, v-head, 128 state rows); one
-// persistent CTA of 256 threads per SM.
+// window T <= 8 (an instance for windows of at most 4 and one for 8, so that
+// the per-window code of the common case is half as long).  A unit is (batch
+// row, v-head, 128 state rows); one persistent CTA of 256 threads per SM.
 //
 // The math is the GDN verify's output-side UT transform with the scalar decay
 // replaced by a vector: with alpha_u = exp(g_u) per channel and
@@ -87,6 +88,9 @@ __device__ __forceinline__ uint32_t sw_f32(int atom, int row, int k) {
 }
 __device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
+// TM: the largest window the instance takes (4 or 8); the shared-memory F and
+// c tables keep their kTMax stride either way
+template <int TM>
 __global__ void __launch_bounds__(kThreads, 1)
 verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, CursorArgs C,
                   const int32_t *__restrict__ slot_idx, int nunits,
@@ -211,13 +215,13 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
             be_in = P.ring_beta[sh_hv * L + ring_pos(base, tid, L)];
         else if (tid < n)
             be_in = bf(bgate + ((size_t)bb * T + (tid - W)) * HV + hv);
-        float vwin[kTMax];
+        float vwin[TM];
 #pragma unroll
-        for (int s = 0; s < kTMax; ++s) vwin[s] = 0.0f;
-        __nv_bfloat16 vraw[kTMax];
+        for (int s = 0; s < TM; ++s) vwin[s] = 0.0f;
+        __nv_bfloat16 vraw[TM];
         if (grp == 1 && vrow < V) {
 #pragma unroll
-            for (int s = 0; s < kTMax; ++s)
+            for (int s = 0; s < TM; ++s)
                 if (s < T) vraw[s] = v[(((size_t)bb * T + s) * HV + hv) * V + vrow];
         }
         const float alog = A_log[hv];
@@ -270,7 +274,7 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
         }
         if (grp == 1 && vrow < V) {
 #pragma unroll
-            for (int s = 0; s < kTMax; ++s)
+            for (int s = 0; s < TM; ++s)
                 if (s < T) {
                     vwin[s] = __bfloat162float(vraw[s]);
                     rawv_w[(sh_hv * L + ring_pos(base, W + s, L)) * V + vrow] = vraw[s];
@@ -502,7 +506,7 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
             // ---- 4. M (I + A) = F^T: the T right-hand sides, s in warp s % 4
             //         (warps 0..3); lane l ends with M[s][l], M[s][l+32]
             if (warp < 4) {
-                constexpr int SPW = kTMax / 4;
+                constexpr int SPW = TM / 4;
                 float f0[SPW], f1[SPW];
 #pragma unroll
                 for (int qq = 0; qq < SPW; ++qq) {
@@ -579,31 +583,34 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
                                            rawv + (sh_hv * L + ring_pos(base, jj, L)) * V + v0, kBV * 2, bar_vh);
                 }
             }
-            float vt[kTMax];
+            float vt[TM];
 #pragma unroll
-            for (int s = 0; s < kTMax; ++s) vt[s] = 0.0f;
+            for (int s = 0; s < TM; ++s) vt[s] = 0.0f;
             if (grp == 0) {
                 // ---- 6. q_eff (thread = key channel):
                 //         eG_{W+s} q^_s - sum_j c[j][s] eG_j k^_j, eG running
                 const int kk = row;
-                float acc[kTMax], eW[kTMax];
+                float acc[TM], eW[TM];
 #pragma unroll
-                for (int s = 0; s < kTMax; ++s) acc[s] = eW[s] = 0.0f;
+                for (int s = 0; s < TM; ++s) acc[s] = eW[s] = 0.0f;
                 float e = 1.0f;
                 for (int j = 0; j < n; ++j) {
                     e *= al[j * K + kk];
                     const float x = e * bf(X + j * K + kk) * rn[j];
-                    const float4 c0 = *reinterpret_cast<const float4 *>(Cm + j * kTMax);
-                    const float4 c1 = *reinterpret_cast<const float4 *>(Cm + j * kTMax + 4);
-                    const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    float cj[TM];
 #pragma unroll
-                    for (int s = 0; s < kTMax; ++s) {
+                    for (int q4 = 0; q4 < TM / 4; ++q4) {
+                        const float4 c = *reinterpret_cast<const float4 *>(Cm + j * kTMax + 4 * q4);
+                        cj[4 * q4] = c.x; cj[4 * q4 + 1] = c.y; cj[4 * q4 + 2] = c.z; cj[4 * q4 + 3] = c.w;
+                    }
+#pragma unroll
+                    for (int s = 0; s < TM; ++s) {
                         acc[s] = fmaf(-cj[s], x, acc[s]);
                         if (j == W + s) eW[s] = e;
                     }
                 }
 #pragma unroll
-                for (int s = 0; s < kTMax; ++s)
+                for (int s = 0; s < TM; ++s)
                     if (s < T) {
                         const float qe = acc[s] + eW[s] * bf(X + (kQRow + s) * K + kk) * rn[kQRow + s];
                         *reinterpret_cast<float *>(sm + kOffQ + sw_f32(kQAtom, s, kk)) = qe;
@@ -619,20 +626,26 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
                     const __nv_bfloat16 *vh = reinterpret_cast<const __nv_bfloat16 *>(sm + kOffR);
                     for (int jj = 0; jj < W; ++jj) {
                         const float x = __bfloat162float(vh[jj * kBV + row]);
-                        const float4 c0 = *reinterpret_cast<const float4 *>(Cm + jj * kTMax);
-                        const float4 c1 = *reinterpret_cast<const float4 *>(Cm + jj * kTMax + 4);
-                        const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                        float cj[TM];
 #pragma unroll
-                        for (int s = 0; s < kTMax; ++s) vt[s] = fmaf(cj[s], x, vt[s]);
+                        for (int q4 = 0; q4 < TM / 4; ++q4) {
+                            const float4 c = *reinterpret_cast<const float4 *>(Cm + jj * kTMax + 4 * q4);
+                            cj[4 * q4] = c.x; cj[4 * q4 + 1] = c.y; cj[4 * q4 + 2] = c.z; cj[4 * q4 + 3] = c.w;
+                        }
+#pragma unroll
+                        for (int s = 0; s < TM; ++s) vt[s] = fmaf(cj[s], x, vt[s]);
                     }
 #pragma unroll
-                    for (int s2 = 0; s2 < kTMax; ++s2) {
+                    for (int s2 = 0; s2 < TM; ++s2) {
                         if (s2 < T) {
-                            const float4 c0 = *reinterpret_cast<const float4 *>(Cm + (W + s2) * kTMax);
-                            const float4 c1 = *reinterpret_cast<const float4 *>(Cm + (W + s2) * kTMax + 4);
-                            const float cj[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                            float cj[TM];
 #pragma unroll
-                            for (int s = 0; s < kTMax; ++s) vt[s] = fmaf(cj[s], vwin[s2], vt[s]);
+                            for (int q4 = 0; q4 < TM / 4; ++q4) {
+                                const float4 c = *reinterpret_cast<const float4 *>(Cm + (W + s2) * kTMax + 4 * q4);
+                                cj[4 * q4] = c.x; cj[4 * q4 + 1] = c.y; cj[4 * q4 + 2] = c.z; cj[4 * q4 + 3] = c.w;
+                            }
+#pragma unroll
+                            for (int s = 0; s < TM; ++s) vt[s] = fmaf(cj[s], vwin[s2], vt[s]);
                         }
                     }
                 }
@@ -670,7 +683,7 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
                 ptx::tmem_ld_wait();
                 if (!stop2 && !stop3 && vrow < V) {
 #pragma unroll
-                    for (int s = 0; s < kTMax; ++s)
+                    for (int s = 0; s < TM; ++s)
                         if (s < T)
                             out[(((size_t)bb * T + s) * HV + hv) * V + vrow] = __float2bfloat16_rn(P.scale * (pr8[s] + vt[s]));
                 }
@@ -728,8 +741,11 @@ std::mutex g_mu_k;
 cudaError_t setup_k(int dev, int *grid) {
     std::lock_guard<std::mutex> lk(g_mu_k);
     if (!g_grid_k[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(ktc::verify_kda_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(ktc::verify_kda_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              ktc::kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ktc::verify_kda_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     ktc::kSmemBytes);
         if (e != cudaSuccess) return e;
         int sms = 0;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -769,7 +785,8 @@ cudaError_t launch_verify_kda_tc(const LayerArgs &P, const CursorArgs &C, const 
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    ktc::verify_kda_kernel<<<grid, ktc::kThreads, ktc::kSmemBytes, stream>>>(
+    auto kern = P.T <= 4 ? ktc::verify_kda_kernel<4> : ktc::verify_kda_kernel<8>;
+    kern<<<grid, ktc::kThreads, ktc::kSmemBytes, stream>>>(
         tmap, P, C, slot_idx, nunits, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
         static_cast<const __nv_bfloat16 *>(v), static_cast<const __nv_bfloat16 *>(a),
         static_cast<const __nv_bfloat16 *>(b), A_log, dt_bias, static_cast<__nv_bfloat16 *>(out), data_wait_limit());
