@@ -197,18 +197,20 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
         // gates: thread = (4 channels, tokens j0, j0 + 8, ...): the ring's g
         // for history tokens, the raw a (element loads: a and dt_bias carry no
         // alignment promise) for window tokens
+        // (a thread's tokens are 8 apart, so at most one of them is in the window)
         const int c4 = 4 * (tid & 31), j0 = tid >> 5;
         float4 gv[kLMax / 8];
 #pragma unroll
         for (int m = 0; m < kLMax / 8; ++m) {
             const int j = j0 + 8 * m;
             gv[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < W) {
-                gv[m] = *reinterpret_cast<const float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4);
-            } else if (j < n) {
-                const __nv_bfloat16 *ar = a + (((size_t)bb * T + (j - W)) * HV + hv) * K + c4;
-                gv[m] = make_float4(bf(ar), bf(ar + 1), bf(ar + 2), bf(ar + 3));
-            }
+            if (j < W) gv[m] = *reinterpret_cast<const float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4);
+        }
+        const int jw = W + ((j0 - W) & 7);   // this thread's window token, if jw < n
+        float4 aw = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (jw < n) {
+            const __nv_bfloat16 *ar = a + (((size_t)bb * T + (jw - W)) * HV + hv) * K + c4;
+            aw = make_float4(bf(ar), bf(ar + 1), bf(ar + 2), bf(ar + 3));
         }
         float be_in = 0.0f;
         if (tid < W)
@@ -255,14 +257,15 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
 #pragma unroll
         for (int m = 0; m < kLMax / 8; ++m) {
             const int j = j0 + 8 * m;
-            if (j >= n) continue;
-            float4 g = gv[m];
-            if (j >= W) {   // the window's gate, written to the ring (side channel)
-                g = make_float4(gate_g(alog, g.x, dtb4.x), gate_g(alog, g.y, dtb4.y), gate_g(alog, g.z, dtb4.z),
-                                gate_g(alog, g.w, dtb4.w));
-                if (vb == 0) *reinterpret_cast<float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, j, L)) * K + c4) = g;
-            }
+            if (j >= W) continue;
+            const float4 g = gv[m];
             *reinterpret_cast<float4 *>(al + j * K + c4) = make_float4(expf(g.x), expf(g.y), expf(g.z), expf(g.w));
+        }
+        if (jw < n) {   // the window's gate, written to the ring (side channel)
+            const float4 g = make_float4(gate_g(alog, aw.x, dtb4.x), gate_g(alog, aw.y, dtb4.y),
+                                         gate_g(alog, aw.z, dtb4.z), gate_g(alog, aw.w, dtb4.w));
+            if (vb == 0) *reinterpret_cast<float4 *>(P.ring_g + (sh_hv * L + ring_pos(base, jw, L)) * K + c4) = g;
+            *reinterpret_cast<float4 *>(al + jw * K + c4) = make_float4(expf(g.x), expf(g.y), expf(g.z), expf(g.w));
         }
         if (tid < n) {
             float be = be_in;
