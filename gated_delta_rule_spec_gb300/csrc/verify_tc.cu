@@ -847,7 +847,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                                      dt_bias, R);
         }
         if (tiles) {
-#pragma unroll
+            // (kept rolled: one copy of the tile, MMA and output code serves both
+            // heads, which keeps the body's instruction footprint smaller)
+#pragma unroll 1
             for (int hh = 0; hh < NH; ++hh) {
                 const bool s0_ok = ptx::mbar_wait(bar_s0, ph_s0, tile_wait_limit);
                 ph_s0 ^= 1u;
@@ -890,7 +892,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curso
                     for (int s = 0; s < TM; ++s)
                         if (s < T)
                             out[(((size_t)bb * T + s) * HV + hv0 + hh) * V + vrow] =
-                                __float2bfloat16_rn(P.scale * (pr8[s] + vt[hh][s]));
+                                __float2bfloat16_rn(P.scale * (pr8[s] + (NH > 1 && hh ? vt[NH - 1][s] : vt[0][s])));
                 }
             }
         }
