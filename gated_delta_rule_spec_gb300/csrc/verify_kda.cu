@@ -506,6 +506,26 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
             stop = true;
         }
         if (!stop) {
+            // ---- 5. the v history into the dead R operands (bulk copies), issued
+            //         by warp 4 while warps 0..3 solve
+            if (warp == 4 && W > 0) {
+                ptx::fence_proxy_async_smem();
+                if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)(W * kBV * 2));
+                __syncwarp();
+                if (V == kBV) {
+                    if (lane == 0) {
+                        const int n1 = (L - base) < W ? (L - base) : W;
+                        ptx::bulk_copy_g2s(sm_s + kOffR, rawv + (sh_hv * L + base) * V, n1 * kBV * 2, bar_vh);
+                        if (W > n1)
+                            ptx::bulk_copy_g2s(sm_s + kOffR + n1 * kBV * 2, rawv + sh_hv * L * V, (W - n1) * kBV * 2,
+                                               bar_vh);
+                    }
+                } else {
+                    for (int jj = lane; jj < W; jj += 32)
+                        ptx::bulk_copy_g2s(sm_s + kOffR + jj * kBV * 2,
+                                           rawv + (sh_hv * L + ring_pos(base, jj, L)) * V + v0, kBV * 2, bar_vh);
+                }
+            }
             // ---- 4. M (I + A) = F^T: the T right-hand sides, s in warp s % 4
             //         (warps 0..3); lane l ends with M[s][l], M[s][l+32]
             if (warp < 4) {
@@ -567,25 +587,6 @@ verify_kda_kernel(const __grid_constant__ CUtensorMap tmap_s0, LayerArgs P, Curs
             }
             __syncthreads();
 
-            // ---- 5. the v history into the dead R operands (bulk copies)
-            if (warp == 4 && W > 0) {
-                ptx::fence_proxy_async_smem();
-                if (lane == 0) ptx::mbar_expect_tx(bar_vh, (uint32_t)(W * kBV * 2));
-                __syncwarp();
-                if (V == kBV) {
-                    if (lane == 0) {
-                        const int n1 = (L - base) < W ? (L - base) : W;
-                        ptx::bulk_copy_g2s(sm_s + kOffR, rawv + (sh_hv * L + base) * V, n1 * kBV * 2, bar_vh);
-                        if (W > n1)
-                            ptx::bulk_copy_g2s(sm_s + kOffR + n1 * kBV * 2, rawv + sh_hv * L * V, (W - n1) * kBV * 2,
-                                               bar_vh);
-                    }
-                } else {
-                    for (int jj = lane; jj < W; jj += 32)
-                        ptx::bulk_copy_g2s(sm_s + kOffR + jj * kBV * 2,
-                                           rawv + (sh_hv * L + ring_pos(base, jj, L)) * V + v0, kBV * 2, bar_vh);
-                }
-            }
             float vt[TM];
 #pragma unroll
             for (int s = 0; s < TM; ++s) vt[s] = 0.0f;
