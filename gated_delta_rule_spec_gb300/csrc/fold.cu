@@ -15,8 +15,8 @@
 // are reduced over the group by a reduce-scatter: two shuffles split the
 // rows between the threads (each keeps two rows' sums, then one), a third
 // finishes the sum (at K = 32 the two splits do), each thread computes the
-// delta of the row it ends with,
-// and four shuffles hand the deltas to the group.  The keys stay in shared
+// delta of the row it ends with, and four shuffles hand the deltas to the
+// group.  The keys stay in shared
 // memory as the raw I/O-dtype records (bf16: half the bytes of fp32) and are
 // widened in registers: per record and state row this reads 64 bytes of
 // keys.  The elementwise work uses Blackwell's packed fp32x2 instructions.
@@ -34,8 +34,10 @@
 // Only the rows whose is_flush is set do any work, and in steady state that
 // is a small share of the batch per step.  So the grid is persistent: every
 // CTA scans the batch's flags, builds the same compact list of slots to
-// fold, and takes work items (row, layer, v-head, block of 32 state rows)
-// round-robin from it.  An item's keys (one or two contiguous ring segments)
+// fold, and takes work items (row, layer, v-head, block of 32 state rows; 64
+// with per-channel decays) round-robin from it.  The kernel is launched
+// dependent on the commit before it in the stream and waits on that grid
+// before its first global access.  An item's keys (one or two contiguous ring segments)
 // and values (one short run per record) arrive by bulk asynchronous copies
 // on an mbarrier while the CTA reads the gates and loads its state rows into
 // registers.  Folding runs after sampling, outside the forward, so the
