@@ -1,7 +1,10 @@
 // cursors.cu -- device-side cursor arithmetic (commit, fold's cursor move,
 // reset).  Pure integer work on [num_slots] arrays, read and written on the
 // device so the whole decode step stays capturable in a CUDA graph (blog post
-// on sglang PR #28695, §1.3 and appendix A.2).
+// on sglang PR #28695, §1.3 and appendix A.2).  The commit and the cursor move
+// are launched dependent on the kernel before them (launch_setup.cuh): each
+// waits on that grid before reading anything and lets the next kernel start
+// its launch right after.
 #include "common.cuh"
 #include "launch_setup.cuh"
 

@@ -1,7 +1,9 @@
-// launch_setup.cuh -- per-device launch set-up of a kernel, kept between calls:
-// the SM count (read once) and the dynamic shared-memory limit (raised only
-// when a call needs more than an earlier one), so that a launch costs no
-// attribute calls once a device has seen its shapes.
+// launch_setup.cuh -- launch helpers of the non-verify kernels: the per-device
+// set-up of a kernel, kept between calls (the SM count, read once, and the
+// dynamic shared-memory limit, raised only when a call needs more than an
+// earlier one), so that a launch costs no attribute calls once a device has
+// seen its shapes; and programmatic dependent launch for the short kernels
+// of a step.
 #pragma once
 
 #include <cstddef>
