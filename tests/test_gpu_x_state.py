@@ -23,7 +23,7 @@ import torch
 import oracle
 from gated_delta_rule_spec_gb300 import binding
 from gated_delta_rule_spec_gb300 import inputs as gen
-from tests.harness import CKPT_REL_FRO, Scenario, to_dev, to_host
+from tests.harness import CKPT_REL_FRO, Scenario, to_host
 
 pytestmark = pytest.mark.gpu
 WL = gen.WORKLOADS

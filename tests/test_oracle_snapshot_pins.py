@@ -6,7 +6,6 @@ import numpy as np
 import pytest
 
 import oracle
-from gated_delta_rule_spec_gb300 import inputs as gen
 from tests.test_oracle_prefill_pins import _dense_prefill, _inputs, _layer
 
 
